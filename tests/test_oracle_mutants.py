@@ -1,0 +1,60 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each mutant is a one-line edit of oracle/pgqa_oracle.c (a dropped term, a
+wrong sign or index, a swapped operand), compiled into a temporary library on
+the CPU.  If a mutant passed every pin, the pins would not be strong enough to
+trust the oracle against that kind of mistake.
+"""
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    "kv_head_modulo": ("const int kvh = h / g;\n    const int d = p->d;",
+                       "const int kvh = h % p->Hkv;\n    const int d = p->d;"),
+    "no_max_shift_in_lse": ("*lse = m + log(z);\n    free(w);", "*lse = log(z);\n    free(w);"),
+    "missing_normalisation": ("o[c] = acc / z;", "o[c] = acc;"),
+    "values_from_keys": ("acc += w[j - j0] * V[j * d + c];", "acc += w[j - j0] * K[j * d + c];"),
+    "page_ignores_indptr": ("int64_t page = kv_indices[kv_indptr[b] + j / page_size];",
+                            "int64_t page = kv_indices[j / page_size];"),
+    "offset_not_modulo": ("int64_t off = j % page_size;", "int64_t off = (j + 1) % page_size;"),
+    "causal_off_by_one": ("allowed = n - L + i + 1;\n            if (allowed < 0) allowed = 0;\n"
+                          "            if (allowed > n) allowed = n;\n        }\n        for",
+                          "allowed = n - L + i;\n            if (allowed < 0) allowed = 0;\n"
+                          "            if (allowed > n) allowed = n;\n        }\n        for"),
+    "causal_top_left": ("allowed = n - L + i + 1;\n            if (allowed < 0) allowed = 0;\n"
+                        "            if (allowed > n) allowed = n;\n        }\n        for",
+                        "allowed = i + 1;\n            if (allowed < 0) allowed = 0;\n"
+                        "            if (allowed > n) allowed = n;\n        }\n        for"),
+    "merge_unnormalised": ("double w = exp(lse_parts[s] - m) / z;", "double w = exp(lse_parts[s] - m);"),
+    "merge_lse_drops_max": ("*lse = m + log(z);\n}", "*lse = log(z);\n}"),
+    "scale_one_over_d": ("scale = 1.0 / sqrt((double)d);\n    problem_t",
+                         "scale = 1.0 / (double)d;\n    problem_t"),
+    "kv_len_whole_pages": ("return (npages - 1) * page_size + last_page_len[b];",
+                           "return (npages - 1) * page_size + last_page_len[b] - 1;"),
+    "fp16_bias": ("v = ldexp((double)(1024 + m), e - 25);", "v = ldexp((double)(1024 + m), e - 24);"),
+    "bf16_shift": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
+    "append_v_from_k": ("memcpy(v_pool + s * row_bytes, v + t * row_bytes",
+                        "memcpy(v_pool + s * row_bytes, k + t * row_bytes"),
+    "softmax_sign": ("w[j - j0] = exp(w[j - j0] - m);", "w[j - j0] = exp(m - w[j - j0]);"),
+    "query_head_index": ("qv[c] = oracle_widen(p->q[(r * p->Hq + h) * (int64_t)d + c], p->dtype);",
+                         "qv[c] = oracle_widen(p->q[(r * p->Hq + (h / g) * g) * (int64_t)d + c], p->dtype);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.SOURCE.read_text()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/present"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    orc = oracle.Oracle(oracle.build(mutated, tmp_path / "libmutant.so", force=True))
+    caught = []
+    for pin_name, pin in sorted(oracle_pins.PINS.items()):
+        try:
+            pin(orc)
+        except (AssertionError, ValueError):
+            caught.append(pin_name)
+    assert caught, f"mutant {name} passed every pin"
