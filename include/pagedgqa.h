@@ -1,0 +1,212 @@
+/*
+ * pagedgqa.h -- C ABI of the GB300 (sm_103a) paged GQA split-KV decode library.
+ *
+ * Decode attention over a paged KV cache with grouped-query heads: each query
+ * row (Hq heads, Hq/Hkv of them sharing each KV head) attends over its
+ * request's cached keys/values, which sit in fixed-size pages of a pool and are
+ * found through a CSR page table.  Work is split along each request's history
+ * ("split-KV"); a partial (output, log-sum-exp) is computed per slice in
+ * parallel and the partials are merged.  A paged KV append writes new tokens'
+ * rows into the pool.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless the parameter name ends in _host.
+ *     The caller owns every buffer it passes; the library never frees them.
+ *   - All work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  No entry point synchronises the device unless it says so.
+ *   - Errors are returned as pgqa_status; nothing traps or aborts.  A failed
+ *     call enqueues no work.  pgqa_last_error() gives a one-line reason
+ *     (thread-local, valid until the next failing call on the same thread).
+ *   - Layouts are row-major and contiguous:
+ *       KV pool   [num_pages, page_size, num_kv_heads, head_dim]  (one for K, one for V)
+ *       q, out    [total_q_rows, num_qo_heads, head_dim]
+ *       lse       [total_q_rows, num_qo_heads]  fp32, natural log
+ *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ *   - Supported shapes: head_dim 64 or 128; page_size 16, 32, 64, 128 or 256;
+ *     num_qo_heads / num_kv_heads between 1 and 8; bf16 or fp16 q/k/v.
+ *     Anything else returns PGQA_ERR_UNSUPPORTED.
+ *   - Pool, q, k, v and out pointers must be 16-byte aligned.
+ */
+#ifndef PAGEDGQA_H
+#define PAGEDGQA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PGQA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define PGQA_API __attribute__((visibility("default")))
+#else
+#define PGQA_API
+#endif
+
+/* Same object as cudaStream_t; declared here so callers need no CUDA headers. */
+typedef struct CUstream_st *pgqa_stream_t;
+
+typedef enum pgqa_status {
+    PGQA_OK = 0,
+    PGQA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, negative size, ... */
+    PGQA_ERR_UNSUPPORTED = 2,    /* shape or dtype outside the supported set */
+    PGQA_ERR_BAD_PAGE_TABLE = 3, /* page table rejected by the host-side check */
+    PGQA_ERR_CUDA = 4,           /* a CUDA runtime call failed */
+    PGQA_ERR_CAPACITY = 5,       /* request exceeds the plan's configured capacity */
+    PGQA_ERR_DEVICE_CHECK = 6    /* a device-side bounds check fired (see pgqa_read_device_flags) */
+} pgqa_status;
+
+typedef enum pgqa_dtype { PGQA_BF16 = 0, PGQA_FP16 = 1, PGQA_FP32 = 2 } pgqa_dtype;
+
+/* Bits of the per-device flag word that kernels set instead of trapping. */
+#define PGQA_FLAG_PAGE_INDEX 1u   /* a page index >= num_pages was skipped */
+#define PGQA_FLAG_SLOT_RANGE 2u   /* an append slot >= num_pages * page_size was skipped */
+#define PGQA_FLAG_WAIT_TIMEOUT 4u /* a pipeline barrier wait gave up (bounded spin) */
+
+PGQA_API int pgqa_abi_version(void);
+PGQA_API const char *pgqa_status_string(pgqa_status status);
+PGQA_API const char *pgqa_last_error(void);
+
+/*
+ * Reads (and with clear != 0 resets) the flag word of the current device.
+ * Synchronises the device.  Returns PGQA_ERR_DEVICE_CHECK when any flag is set.
+ */
+PGQA_API pgqa_status pgqa_read_device_flags(uint32_t *flags_host, int clear);
+
+/*
+ * pgqa_kv_append -- paged KV append.
+ *
+ * Defined by the "flashlet" README, design bullets: the pool is laid out
+ * [pages, page_size, kv_heads, head_dim] (FlashInfer's NHD) so that writing new
+ * tokens is a single index copy of their rows into flat slots.
+ *
+ *   k_pool, v_pool  pools [num_pages, page_size, num_kv_heads, head_dim], dtype
+ *   k, v            new rows [num_tokens, num_kv_heads, head_dim], dtype
+ *   slot_mapping    [num_tokens] int64, device; row t goes to flat slot
+ *                   slot_mapping[t] = page * page_size + offset.  A negative
+ *                   slot skips the row (padding).  A slot >= num_pages*page_size
+ *                   is skipped and raises PGQA_FLAG_SLOT_RANGE.  Two rows with
+ *                   the same slot in one call race (undefined which one lands).
+ * The copy is bit-exact.  num_tokens == 0 enqueues nothing.
+ */
+PGQA_API pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_pages, int page_size,
+                           int num_kv_heads, int head_dim, pgqa_dtype dtype,
+                           const void *k, const void *v, const int64_t *slot_mapping,
+                           int64_t num_tokens, pgqa_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* plan / run                                                                */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The plan()/run() split follows the "flashlet" README (backends/base.py:
+ * AttentionBackend ABC with plan() / run(); design bullets: metadata in
+ * persistent device buffers updated in place each step).  A plan owns device
+ * buffers sized once at creation (work list, merge list, split partials), so
+ * their addresses never change and run() can be captured in a CUDA graph.
+ */
+typedef struct pgqa_plan pgqa_plan;
+
+typedef struct pgqa_plan_config {
+    int num_qo_heads;     /* Hq */
+    int num_kv_heads;     /* Hkv; Hq % Hkv == 0 */
+    int head_dim;         /* 64 or 128 */
+    int page_size;        /* 16, 32, 64, 128 or 256 */
+    pgqa_dtype dtype;     /* q/k/v element type: PGQA_BF16 or PGQA_FP16 */
+    int max_batch;        /* most requests one plan_update may describe */
+    int64_t max_q_rows;   /* most query rows one run may carry (decode + prefill rows) */
+    int max_splits;       /* cap on slices per (request, kv head); 0 = no cap; 1 = never split */
+    int split_tokens;     /* > 0 forces this slice length (rounded up to the kernel tile);
+                             0 = choose it so that the slices fill the SMs */
+    int ctas_per_sm;      /* occupancy target of the split heuristic; 0 = library default */
+} pgqa_plan_config;
+
+/*
+ * Creates a plan on the current device.  Allocates its device and pinned host
+ * buffers (the only allocations the library makes).  *plan is set to NULL on
+ * failure.
+ */
+PGQA_API pgqa_status pgqa_plan_create(pgqa_plan **plan, const pgqa_plan_config *cfg);
+
+/*
+ * pgqa_plan_update -- plan().
+ *
+ * Split-KV as in "A library kernel for decode", section "What changed": each
+ * request's cached keys are cut into slices, one partial per slice is computed
+ * in parallel and the partials are merged, so one request's history spreads
+ * over many SMs.  The slice length is chosen here, from the kv lengths, so
+ * that the slices of all requests fill the GPU's SMs.
+ *
+ *   kv_indptr_host      [batch+1] int32, host; pages of request b are
+ *                       kv_indices[kv_indptr[b] .. kv_indptr[b+1])
+ *   last_page_len_host  [batch] int32, host; rows used in the request's last
+ *                       page, in [1, page_size], or 0 for a request with no pages.
+ *                       kv_len(b) = (npages - 1) * page_size + last_page_len[b].
+ *   qo_indptr_host      [batch+1] int32, host, or NULL.  NULL: request b owns
+ *                       exactly query row b (pure decode).  Otherwise request b
+ *                       owns rows qo_indptr[b] .. qo_indptr[b+1] (the ragged
+ *                       form of the "flashlet" README, design bullets:
+ *                       qo_indptr lengths [512, 1, 1, ...] in one call).
+ *   kv_indices          [kv_indptr[batch]] int32, DEVICE; must stay valid and
+ *                       unchanged until the last run() that uses this plan.
+ *   kv_indices_host     optional host mirror of kv_indices (NULL allowed).  When
+ *                       given, every index is checked here against num_pages;
+ *                       when not, the kernels skip out-of-range pages and raise
+ *                       PGQA_FLAG_PAGE_INDEX.
+ *   num_pages           pages in each pool
+ *   causal              for rows of a request with L query rows over N keys, row
+ *                       i may attend keys j <= N - L + i (bottom-right).  It has
+ *                       no effect on single-row (decode) requests.
+ * The host arrays are read before the call returns.  One asynchronous copy of
+ * the work list into the plan's device buffer is enqueued on `stream`; a
+ * run() on another stream must be ordered after it by the caller.
+ * Errors: PGQA_ERR_BAD_PAGE_TABLE (non-monotone indptr or qo_indptr,
+ * last_page_len out of range, index out of range when a host mirror is
+ * given), PGQA_ERR_CAPACITY (batch, rows or work items beyond the configured
+ * maxima).
+ */
+PGQA_API pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr_host,
+                             const int32_t *last_page_len_host, const int32_t *qo_indptr_host,
+                             int batch, const int32_t *kv_indices,
+                             const int32_t *kv_indices_host, int64_t num_pages, int causal,
+                             pgqa_stream_t stream);
+
+/*
+ * pgqa_run -- run(): attention for every query row of the last plan_update.
+ *
+ *   q          [total_q_rows, Hq, head_dim], the plan's dtype
+ *   k_pool     [num_pages, page_size, Hkv, head_dim], the plan's dtype
+ *   v_pool     same shape
+ *   out        [total_q_rows, Hq, head_dim] of out_dtype (the plan's dtype or PGQA_FP32)
+ *   lse        [total_q_rows, Hq] fp32 natural-log log-sum-exp of the scaled
+ *              scores, or NULL.  A row with no key gets out = 0, lse = -inf.
+ *   sm_scale   score scale; <= 0 selects 1/sqrt(head_dim)
+ * Launches the split-KV partial kernel and, when some row was split, the
+ * merge kernel.  Outputs are bit-for-bit repeatable for the same plan and inputs.
+ */
+PGQA_API pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const void *v_pool,
+                     void *out, pgqa_dtype out_dtype, float *lse, float sm_scale,
+                     pgqa_stream_t stream);
+
+/* Frees the plan's buffers (synchronising with its last enqueued copy).  NULL is a no-op. */
+PGQA_API pgqa_status pgqa_plan_destroy(pgqa_plan *plan);
+
+/* What the last plan_update decided (host-side, no synchronisation). */
+typedef struct pgqa_plan_info {
+    int num_items;          /* CTAs of the partial kernel */
+    int num_merge_tasks;    /* (query row, kv head) pairs whose slices are merged */
+    int split_tokens;       /* slice length used */
+    int max_splits_used;    /* most slices any (request, kv head) got */
+    int total_q_rows;
+    int num_sms;            /* SMs of the plan's device */
+    int64_t kv_tokens;      /* sum of kv_len over requests */
+} pgqa_plan_info;
+
+PGQA_API pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDGQA_H */

@@ -1,1 +1,7 @@
-"""Placeholder; the binding is added with the library."""
+"""GB300 (sm_103a) paged GQA split-KV decode attention with a C ABI.
+
+The compute lives in ``_build/libpagedgqa.so`` (hand-written CUDA); this package
+only marshals torch tensors into its C entry points (see include/pagedgqa.h).
+"""
+from .binding import (BF16, FP16, FP32, PagedGQAError, Plan, kv_append, load, plan_create,  # noqa: F401
+                      plan_destroy, plan_get_info, plan_update, read_device_flags, run)

@@ -1,0 +1,244 @@
+"""Thin ctypes binding of libpagedgqa.so (argument marshalling only).
+
+The functions carry the C ABI's names without the ``pgqa_`` prefix:
+``kv_append``, ``plan_create``, ``plan_update``, ``run``, ``plan_destroy``,
+``plan_get_info``, ``read_device_flags``.  Every step of the computation runs in
+the library's CUDA kernels; torch only supplies device memory and the stream.
+There is no fallback: if the shared library is missing or fails to load, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Optional
+
+import numpy as np
+import torch
+
+LIBRARY = Path(__file__).resolve().parent / "_build" / "libpagedgqa.so"
+
+BF16, FP16, FP32 = 0, 1, 2
+TORCH_TO_CODE = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}
+CODE_TO_TORCH = {v: k for k, v in TORCH_TO_CODE.items()}
+
+STATUS_NAMES = {0: "PGQA_OK", 1: "PGQA_ERR_INVALID_ARG", 2: "PGQA_ERR_UNSUPPORTED",
+                3: "PGQA_ERR_BAD_PAGE_TABLE", 4: "PGQA_ERR_CUDA", 5: "PGQA_ERR_CAPACITY",
+                6: "PGQA_ERR_DEVICE_CHECK"}
+
+# Every entry point include/pagedgqa.h declares.
+EXPORTS = ("pgqa_abi_version", "pgqa_status_string", "pgqa_last_error", "pgqa_read_device_flags",
+           "pgqa_kv_append", "pgqa_plan_create", "pgqa_plan_update", "pgqa_run",
+           "pgqa_plan_destroy", "pgqa_plan_get_info")
+
+
+class PagedGQAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+
+
+class PlanConfig(ctypes.Structure):
+    _fields_ = [("num_qo_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("max_batch", ctypes.c_int), ("max_q_rows", ctypes.c_int64),
+                ("max_splits", ctypes.c_int), ("split_tokens", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_items", ctypes.c_int), ("num_merge_tasks", ctypes.c_int),
+                ("split_tokens", ctypes.c_int), ("max_splits_used", ctypes.c_int),
+                ("total_q_rows", ctypes.c_int), ("num_sms", ctypes.c_int),
+                ("kv_tokens", ctypes.c_int64)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+
+
+def load(path: Path | str | None = None) -> ctypes.CDLL:
+    """Loads the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = Path(path) if path else LIBRARY
+    if not path.exists():
+        raise RuntimeError(f"{path} is missing: build it with `python -m paged_kv_gqa_05_gb300.build` "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(str(path))
+    lib.pgqa_abi_version.restype = ctypes.c_int
+    lib.pgqa_status_string.restype = ctypes.c_char_p
+    lib.pgqa_status_string.argtypes = [ctypes.c_int]
+    lib.pgqa_last_error.restype = ctypes.c_char_p
+    lib.pgqa_read_device_flags.restype = ctypes.c_int
+    lib.pgqa_read_device_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    lib.pgqa_kv_append.restype = ctypes.c_int
+    lib.pgqa_kv_append.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, _vp, _vp, _vp, ctypes.c_int64, _vp]
+    lib.pgqa_plan_create.restype = ctypes.c_int
+    lib.pgqa_plan_create.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(PlanConfig)]
+    lib.pgqa_plan_update.restype = ctypes.c_int
+    lib.pgqa_plan_update.argtypes = [_vp, _i32p, _i32p, _i32p, ctypes.c_int, _vp, _i32p,
+                                     ctypes.c_int64, ctypes.c_int, _vp]
+    lib.pgqa_run.restype = ctypes.c_int
+    lib.pgqa_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_float, _vp]
+    lib.pgqa_plan_destroy.restype = ctypes.c_int
+    lib.pgqa_plan_destroy.argtypes = [_vp]
+    lib.pgqa_plan_get_info.restype = ctypes.c_int
+    lib.pgqa_plan_get_info.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
+    if lib.pgqa_abi_version() != 1:
+        raise RuntimeError("libpagedgqa.so ABI version mismatch")
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise PagedGQAError(status, load().pgqa_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _host_i32(a, name: str) -> Optional[np.ndarray]:
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda:
+            raise ValueError(f"{name} must be a host array")
+        a = a.numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _i32ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_i32p)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+              slot_mapping: torch.Tensor, stream=None) -> None:
+    """pgqa_kv_append: rows k[t], v[t] -> flat slot slot_mapping[t] of the pools."""
+    P, ps, Hkv, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or k.shape != v.shape or k.shape[1:] != (Hkv, D):
+        raise ValueError("shape mismatch between pools and rows")
+    if k_pool.dtype != k.dtype or v_pool.dtype != k.dtype or v.dtype != k.dtype:
+        raise ValueError("pools and rows must share one dtype")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    lib = load()
+    _check(lib.pgqa_kv_append(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), P, ps, Hkv, D,
+                              TORCH_TO_CODE[k.dtype], _dev(k, "k"), _dev(v, "v"),
+                              _dev(slot_mapping, "slot_mapping"), k.shape[0], _stream(stream)))
+
+
+def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
+                split_tokens: int = 0, ctas_per_sm: int = 0) -> int:
+    """pgqa_plan_create on the current CUDA device; returns the plan handle."""
+    cfg = PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
+                     max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm)
+    h = _vp()
+    _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
+    return h.value
+
+
+def plan_update(plan: int, kv_indptr, last_page_len, kv_indices: torch.Tensor, num_pages: int,
+                qo_indptr=None, kv_indices_host=None, causal: bool = False, stream=None) -> None:
+    """pgqa_plan_update; kv_indptr / last_page_len / qo_indptr / kv_indices_host are host arrays."""
+    indptr = _host_i32(kv_indptr, "kv_indptr")
+    last = _host_i32(last_page_len, "last_page_len")
+    qo = _host_i32(qo_indptr, "qo_indptr")
+    mirror = _host_i32(kv_indices_host, "kv_indices_host")
+    if kv_indices.dtype != torch.int32:
+        raise ValueError("kv_indices must be int32")
+    batch = len(indptr) - 1
+    dptr = _dev(kv_indices, "kv_indices") if kv_indices.numel() else None
+    _check(load().pgqa_plan_update(plan, _i32ptr(indptr), _i32ptr(last), _i32ptr(qo), batch, dptr,
+                                   _i32ptr(mirror), int(num_pages), int(bool(causal)),
+                                   _stream(stream)))
+
+
+def run(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+        out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+        lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """pgqa_run; allocates `out` (torch) when it is not given."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise ValueError("q and pools must share one dtype")
+    _check(load().pgqa_run(plan, _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                           _dev(out, "out"), TORCH_TO_CODE[out.dtype],
+                           None if lse is None else _dev(lse, "lse"), float(sm_scale),
+                           _stream(stream)))
+    return out
+
+
+def plan_destroy(plan: int) -> None:
+    _check(load().pgqa_plan_destroy(plan))
+
+
+def plan_get_info(plan: int) -> dict:
+    info = PlanInfo()
+    _check(load().pgqa_plan_get_info(plan, ctypes.byref(info)))
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+
+
+def read_device_flags(clear: bool = True) -> int:
+    """Flag word of the current device (synchronises).  0 when no check fired."""
+    v = ctypes.c_uint32(0)
+    st = load().pgqa_read_device_flags(ctypes.byref(v), int(clear))
+    if st not in (0, 6):
+        _check(st)
+    return int(v.value)
+
+
+class Plan:
+    """Owns a plan handle; plan()/run() in the style of an attention backend."""
+
+    def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
+                 dtype: torch.dtype, max_batch: int, max_q_rows: int, **options):
+        self.handle = plan_create(num_qo_heads, num_kv_heads, head_dim, page_size, dtype,
+                                  max_batch, max_q_rows, **options)
+        self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+
+    def update(self, *args, **kwargs) -> "Plan":
+        plan_update(self.handle, *args, **kwargs)
+        return self
+
+    def run(self, *args, **kwargs) -> torch.Tensor:
+        return run(self.handle, *args, **kwargs)
+
+    def info(self) -> dict:
+        return plan_get_info(self.handle)
+
+    def close(self) -> None:
+        if self.handle:
+            plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

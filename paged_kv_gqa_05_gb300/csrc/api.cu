@@ -1,0 +1,540 @@
+// C ABI of the library: argument checks, the plan (split heuristic + work list
+// upload into persistent device buffers), TMA descriptor set-up and launches.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+namespace pgqa {
+cudaError_t launch_decode_bf16_d64(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d64(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d128(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+
+cudaError_t launch_decode(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
+                          cudaStream_t stream) {
+    if (dtype == PGQA_BF16)
+        return head_dim == 64 ? launch_decode_bf16_d64(group, tm_k, tm_v, p, num_items, pdl, stream)
+                              : launch_decode_bf16_d128(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return head_dim == 64 ? launch_decode_fp16_d64(group, tm_k, tm_v, p, num_items, pdl, stream)
+                          : launch_decode_fp16_d128(group, tm_k, tm_v, p, num_items, pdl, stream);
+}
+}  // namespace pgqa
+
+using namespace pgqa;
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+static thread_local char g_last_error[512] = "";
+
+static pgqa_status fail(pgqa_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+static pgqa_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(PGQA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------
+// per-device flag word
+// ---------------------------------------------------------------------------
+static __device__ unsigned int g_device_flags;
+
+static pgqa_status device_flags(unsigned int **out) {
+    static std::mutex mu;
+    static unsigned int *ptrs[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 256) return fail(PGQA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_flags);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(flags)");
+        ptrs[dev] = static_cast<unsigned int *>(p);
+    }
+    *out = ptrs[dev];
+    return PGQA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptors
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool [num_pages, page_size, Hkv, D] as the 3-D tensor {D, Hkv, rows};
+// one box is `box_rows` consecutive rows of one kv head.
+static pgqa_status make_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages, int page_size,
+                                 int num_kv_heads, int head_dim, pgqa_dtype dt, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PGQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(num_pages) * page_size};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                   static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, dt == PGQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return PGQA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// helpers
+// ---------------------------------------------------------------------------
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool supported_page_size(int ps) {
+    return ps == 16 || ps == 32 || ps == 64 || ps == 128 || ps == 256;
+}
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// ---------------------------------------------------------------------------
+// plan
+// ---------------------------------------------------------------------------
+struct MapCacheEntry {
+    const void *ptr = nullptr;
+    int64_t num_pages = 0;
+    CUtensorMap map;
+};
+
+struct pgqa_plan {
+    pgqa_plan_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    int group = 0;
+    int tile = 0;       // decode warp tile (tokens)
+    int box_rows = 0;
+    int ctas_per_sm = 0;
+    int max_items = 0;  // capacity of the work list and of the partial slots
+    int max_tasks = 0;
+
+    void *d_meta = nullptr;  // [max_items] WorkItem then [max_tasks] MergeTask
+    float *d_partial_o = nullptr;
+    float *d_partial_lse = nullptr;
+    void *h_meta[2] = {nullptr, nullptr};
+    cudaEvent_t staged[2] = {nullptr, nullptr};
+    bool staged_used[2] = {false, false};
+    int cur = 0;
+
+    bool valid = false;
+    int n_items = 0, n_tasks = 0, split_tokens = 0, max_splits_used = 0, total_q_rows = 0;
+    int max_task_splits = 0;
+    int64_t kv_tokens = 0, num_pages = 0;
+    const int32_t *kv_indices = nullptr;
+
+    static constexpr int kMapCache = 64;
+    MapCacheEntry maps[kMapCache];
+    int map_next = 0;
+
+    WorkItem *items() { return static_cast<WorkItem *>(d_meta); }
+    MergeTask *tasks() {
+        return reinterpret_cast<MergeTask *>(static_cast<char *>(d_meta) + sizeof(WorkItem) * max_items);
+    }
+};
+
+static pgqa_status pool_map(pgqa_plan *plan, const void *pool, const CUtensorMap **out) {
+    for (auto &e : plan->maps)
+        if (e.ptr == pool && e.num_pages == plan->num_pages) {
+            *out = &e.map;
+            return PGQA_OK;
+        }
+    MapCacheEntry &e = plan->maps[plan->map_next];
+    plan->map_next = (plan->map_next + 1) % pgqa_plan::kMapCache;
+    pgqa_status s = make_pool_map(&e.map, pool, plan->num_pages, plan->cfg.page_size, plan->cfg.num_kv_heads,
+                                  plan->cfg.head_dim, plan->cfg.dtype, plan->box_rows);
+    if (s != PGQA_OK) {
+        e.ptr = nullptr;
+        return s;
+    }
+    e.ptr = pool;
+    e.num_pages = plan->num_pages;
+    *out = &e.map;
+    return PGQA_OK;
+}
+
+static void plan_free(pgqa_plan *p) {
+    if (!p) return;
+    for (int i = 0; i < 2; ++i) {
+        if (p->staged[i]) {
+            cudaEventSynchronize(p->staged[i]);
+            cudaEventDestroy(p->staged[i]);
+        }
+        if (p->h_meta[i]) cudaFreeHost(p->h_meta[i]);
+    }
+    if (p->d_meta) cudaFree(p->d_meta);
+    if (p->d_partial_o) cudaFree(p->d_partial_o);
+    if (p->d_partial_lse) cudaFree(p->d_partial_lse);
+    delete p;
+}
+
+extern "C" {
+
+int pgqa_abi_version(void) { return PGQA_ABI_VERSION; }
+
+const char *pgqa_status_string(pgqa_status s) {
+    switch (s) {
+        case PGQA_OK: return "ok";
+        case PGQA_ERR_INVALID_ARG: return "invalid argument";
+        case PGQA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PGQA_ERR_BAD_PAGE_TABLE: return "malformed page table";
+        case PGQA_ERR_CUDA: return "CUDA error";
+        case PGQA_ERR_CAPACITY: return "plan capacity exceeded";
+        case PGQA_ERR_DEVICE_CHECK: return "device-side check fired";
+    }
+    return "unknown status";
+}
+
+const char *pgqa_last_error(void) { return g_last_error; }
+
+pgqa_status pgqa_read_device_flags(uint32_t *flags_host, int clear) {
+    if (!flags_host) return fail(PGQA_ERR_INVALID_ARG, "flags_host is NULL");
+    unsigned int *d = nullptr;
+    pgqa_status s = device_flags(&d);
+    if (s != PGQA_OK) return s;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpy(flags_host, d, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device flags");
+    if (clear) {
+        e = cudaMemset(d, 0, sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "clear device flags");
+    }
+    if (*flags_host) return fail(PGQA_ERR_DEVICE_CHECK, "device flags 0x%x", *flags_host);
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_pages, int page_size, int num_kv_heads,
+                           int head_dim, pgqa_dtype dtype, const void *k, const void *v,
+                           const int64_t *slot_mapping, int64_t num_tokens, pgqa_stream_t stream) {
+    if (num_tokens < 0 || num_pages < 0) return fail(PGQA_ERR_INVALID_ARG, "negative size");
+    if (dtype != PGQA_BF16 && dtype != PGQA_FP16) return fail(PGQA_ERR_UNSUPPORTED, "append dtype must be bf16/fp16");
+    if (head_dim != 64 && head_dim != 128) return fail(PGQA_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (!supported_page_size(page_size)) return fail(PGQA_ERR_UNSUPPORTED, "page_size %d", page_size);
+    if (num_kv_heads < 1) return fail(PGQA_ERR_INVALID_ARG, "num_kv_heads %d", num_kv_heads);
+    if (num_tokens == 0) return PGQA_OK;
+    if (!k_pool || !v_pool || !k || !v || !slot_mapping) return fail(PGQA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k) || !aligned16(v))
+        return fail(PGQA_ERR_INVALID_ARG, "pool and row pointers must be 16-byte aligned");
+    unsigned int *flags = nullptr;
+    pgqa_status s = device_flags(&flags);
+    if (s != PGQA_OK) return s;
+    const int row_bytes = num_kv_heads * head_dim * 2;
+    cudaError_t e = launch_kv_append(k_pool, v_pool, k, v, slot_mapping, num_tokens, num_pages * page_size,
+                                     row_bytes, flags, true, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
+    if (!out || !cfg) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
+    *out = nullptr;
+    const pgqa_plan_config &c = *cfg;
+    if (c.num_kv_heads < 1 || c.num_qo_heads < 1 || c.num_qo_heads % c.num_kv_heads != 0)
+        return fail(PGQA_ERR_INVALID_ARG, "num_qo_heads %d must be a positive multiple of num_kv_heads %d",
+                    c.num_qo_heads, c.num_kv_heads);
+    const int group = c.num_qo_heads / c.num_kv_heads;
+    if (group > 8) return fail(PGQA_ERR_UNSUPPORTED, "query heads per kv head %d > 8", group);
+    if (c.head_dim != 64 && c.head_dim != 128) return fail(PGQA_ERR_UNSUPPORTED, "head_dim %d", c.head_dim);
+    if (!supported_page_size(c.page_size)) return fail(PGQA_ERR_UNSUPPORTED, "page_size %d", c.page_size);
+    if (c.dtype != PGQA_BF16 && c.dtype != PGQA_FP16) return fail(PGQA_ERR_UNSUPPORTED, "dtype must be bf16/fp16");
+    if (c.max_batch < 1 || c.max_q_rows < 1 || c.max_q_rows > (1 << 24))
+        return fail(PGQA_ERR_INVALID_ARG, "max_batch/max_q_rows out of range");
+    if (c.max_splits < 0 || c.split_tokens < 0 || c.ctas_per_sm < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
+
+    pgqa_plan *p = new (std::nothrow) pgqa_plan();
+    if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
+    p->cfg = c;
+    p->group = group;
+    p->tile = decode_warp_tile(c.head_dim);
+    p->box_rows = std::min(c.page_size, p->tile);
+    p->ctas_per_sm = c.ctas_per_sm > 0 ? c.ctas_per_sm : 2;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        plan_free(p);
+        return cuda_fail(e, "device query");
+    }
+    // Slices never exceed (target CTAs) + (one per row and kv head); forced short slices may need more.
+    const int64_t items = c.max_q_rows * c.num_kv_heads + 8LL * p->num_sms * p->ctas_per_sm + 64;
+    if (items > (1 << 26)) {
+        plan_free(p);
+        return fail(PGQA_ERR_CAPACITY, "plan capacity too large");
+    }
+    p->max_items = static_cast<int>(items);
+    p->max_tasks = static_cast<int>(c.max_q_rows * c.num_kv_heads);
+    const size_t meta = sizeof(WorkItem) * p->max_items + sizeof(MergeTask) * p->max_tasks;
+    e = cudaMalloc(&p->d_meta, meta);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&p->d_partial_o),
+                       sizeof(float) * static_cast<size_t>(p->max_items) * group * c.head_dim);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&p->d_partial_lse), sizeof(float) * static_cast<size_t>(p->max_items) * group);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+        e = cudaMallocHost(&p->h_meta[i], meta);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->staged[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        plan_free(p);
+        return cuda_fail(e, "plan allocation");
+    }
+    *out = p;
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_destroy(pgqa_plan *plan) {
+    plan_free(plan);
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info) {
+    if (!plan || !info) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
+    info->num_items = plan->n_items;
+    info->num_merge_tasks = plan->n_tasks;
+    info->split_tokens = plan->split_tokens;
+    info->max_splits_used = plan->max_splits_used;
+    info->total_q_rows = plan->total_q_rows;
+    info->num_sms = plan->num_sms;
+    info->kv_tokens = plan->kv_tokens;
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
+                             const int32_t *qo_indptr, int batch, const int32_t *kv_indices,
+                             const int32_t *kv_indices_host, int64_t num_pages, int causal,
+                             pgqa_stream_t stream) {
+    if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
+    plan->valid = false;
+    const pgqa_plan_config &c = plan->cfg;
+    if (batch < 0 || num_pages < 0) return fail(PGQA_ERR_INVALID_ARG, "negative batch or num_pages");
+    if (batch > c.max_batch) return fail(PGQA_ERR_CAPACITY, "batch %d > max_batch %d", batch, c.max_batch);
+    if (num_pages * static_cast<int64_t>(c.page_size) >= (int64_t(1) << 31))
+        return fail(PGQA_ERR_UNSUPPORTED, "pool rows must stay below 2^31");
+    if (!kv_indptr || (batch > 0 && !last_page_len)) return fail(PGQA_ERR_INVALID_ARG, "NULL page table");
+    if (kv_indptr[0] != 0) return fail(PGQA_ERR_BAD_PAGE_TABLE, "kv_indptr[0] = %d", kv_indptr[0]);
+    for (int b = 0; b < batch; ++b) {
+        const int64_t np = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
+        if (np < 0) return fail(PGQA_ERR_BAD_PAGE_TABLE, "kv_indptr decreases at request %d", b);
+        if (np == 0 && last_page_len[b] != 0)
+            return fail(PGQA_ERR_BAD_PAGE_TABLE, "request %d has no pages but last_page_len %d", b, last_page_len[b]);
+        if (np > 0 && (last_page_len[b] < 1 || last_page_len[b] > c.page_size))
+            return fail(PGQA_ERR_BAD_PAGE_TABLE, "last_page_len[%d] = %d outside [1, %d]", b, last_page_len[b],
+                        c.page_size);
+        if (np * c.page_size >= (int64_t(1) << 30)) return fail(PGQA_ERR_UNSUPPORTED, "request %d too long", b);
+    }
+    const int64_t nnz = batch > 0 ? kv_indptr[batch] : 0;
+    if (nnz > 0 && !kv_indices) return fail(PGQA_ERR_INVALID_ARG, "kv_indices is NULL");
+    if (kv_indices_host)
+        for (int64_t i = 0; i < nnz; ++i)
+            if (kv_indices_host[i] < 0 || kv_indices_host[i] >= num_pages)
+                return fail(PGQA_ERR_BAD_PAGE_TABLE, "kv_indices[%lld] = %d outside [0, %lld)",
+                            static_cast<long long>(i), kv_indices_host[i], static_cast<long long>(num_pages));
+    int64_t rows = batch;
+    if (qo_indptr) {
+        if (qo_indptr[0] != 0) return fail(PGQA_ERR_BAD_PAGE_TABLE, "qo_indptr[0] = %d", qo_indptr[0]);
+        for (int b = 0; b < batch; ++b)
+            if (qo_indptr[b + 1] < qo_indptr[b]) return fail(PGQA_ERR_BAD_PAGE_TABLE, "qo_indptr decreases at %d", b);
+        rows = batch > 0 ? qo_indptr[batch] : 0;
+    }
+    if (rows > c.max_q_rows)
+        return fail(PGQA_ERR_CAPACITY, "%lld query rows > max_q_rows %lld", static_cast<long long>(rows),
+                    static_cast<long long>(c.max_q_rows));
+
+    // Admissible keys per query row (bottom-right causal for multi-row requests).
+    struct Row {
+        int32_t q_row, page_base, n;
+    };
+    std::vector<Row> rowv;
+    rowv.reserve(static_cast<size_t>(rows));
+    int64_t work = 0, kv_tokens = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t np = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
+        const int64_t n = np == 0 ? 0 : (np - 1) * c.page_size + last_page_len[b];
+        kv_tokens += n;
+        const int64_t r0 = qo_indptr ? qo_indptr[b] : b, r1 = qo_indptr ? qo_indptr[b + 1] : b + 1;
+        const int64_t L = r1 - r0;
+        for (int64_t r = r0; r < r1; ++r) {
+            int64_t a = n;
+            if (causal) a = std::min<int64_t>(n, std::max<int64_t>(0, n - L + (r - r0) + 1));
+            rowv.push_back({static_cast<int32_t>(r), kv_indptr[b], static_cast<int32_t>(a)});
+            work += a;
+        }
+    }
+    work *= c.num_kv_heads;
+
+    // Slice length: enough slices to fill num_sms * ctas_per_sm CTAs, each a whole
+    // number of warp tiles and at least one tile per warp.
+    const int tile = plan->tile;
+    const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
+    int64_t ls;
+    if (c.split_tokens > 0) {
+        ls = round_up(c.split_tokens, tile);
+    } else {
+        const int64_t target = static_cast<int64_t>(plan->num_sms) * plan->ctas_per_sm;
+        ls = std::max<int64_t>(min_split, round_up(std::max<int64_t>(1, ceil_div(work, target)), tile));
+    }
+
+    std::vector<WorkItem> items;
+    std::vector<MergeTask> tasks;
+    items.reserve(static_cast<size_t>(rows) * c.num_kv_heads);
+    int slot = 0, max_used = 1, max_task_splits = 0;
+    for (const Row &rw : rowv) {
+        for (int kvh = 0; kvh < c.num_kv_heads; ++kvh) {
+            const int64_t n = rw.n;
+            int64_t ns = n == 0 ? 1 : ceil_div(n, ls);
+            if (c.max_splits > 0) ns = std::min<int64_t>(ns, c.max_splits);
+            const int64_t len = n == 0 ? 0 : round_up(ceil_div(n, ns), tile);
+            ns = n == 0 ? 1 : ceil_div(n, len);
+            if (ns == 1) {
+                items.push_back({rw.page_base, 0, static_cast<int32_t>(n), rw.q_row, kvh, -1, 0, 0});
+                continue;
+            }
+            if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_items)
+                return fail(PGQA_ERR_CAPACITY, "split partials exceed the plan capacity");
+            for (int64_t s = 0; s < ns; ++s)
+                items.push_back({rw.page_base, static_cast<int32_t>(s * len),
+                                 static_cast<int32_t>(std::min<int64_t>(n, (s + 1) * len)), rw.q_row, kvh,
+                                 slot + static_cast<int32_t>(s), 0, 0});
+            tasks.push_back({rw.q_row, kvh, slot, static_cast<int32_t>(ns)});
+            slot += static_cast<int>(ns);
+            max_used = std::max<int>(max_used, static_cast<int>(ns));
+            max_task_splits = std::max<int>(max_task_splits, static_cast<int>(ns));
+        }
+        if (static_cast<int64_t>(items.size()) > plan->max_items)
+            return fail(PGQA_ERR_CAPACITY, "work items exceed the plan capacity %d", plan->max_items);
+    }
+    // Longest slices first, so that they start in the first wave.
+    std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &b) {
+        return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+    });
+
+    // Stage in pinned memory (double-buffered) and copy into the persistent buffer.
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int buf = plan->cur;
+    cudaError_t e = cudaSuccess;
+    if (plan->staged_used[buf]) {
+        e = cudaEventSynchronize(plan->staged[buf]);
+        if (e != cudaSuccess) return cuda_fail(e, "staging buffer wait");
+    }
+    char *h = static_cast<char *>(plan->h_meta[buf]);
+    const size_t items_bytes = sizeof(WorkItem) * items.size();
+    const size_t tasks_off = sizeof(WorkItem) * plan->max_items;
+    const size_t tasks_bytes = sizeof(MergeTask) * tasks.size();
+    if (items_bytes) std::memcpy(h, items.data(), items_bytes);
+    if (tasks_bytes) std::memcpy(h + tasks_off, tasks.data(), tasks_bytes);
+    if (items_bytes) e = cudaMemcpyAsync(plan->d_meta, h, items_bytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && tasks_bytes)
+        e = cudaMemcpyAsync(static_cast<char *>(plan->d_meta) + tasks_off, h + tasks_off, tasks_bytes,
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->staged[buf], st);
+    if (e != cudaSuccess) return cuda_fail(e, "work list upload");
+    plan->staged_used[buf] = true;
+    plan->cur ^= 1;
+
+    plan->n_items = static_cast<int>(items.size());
+    plan->n_tasks = static_cast<int>(tasks.size());
+    plan->split_tokens = static_cast<int>(ls);
+    plan->max_splits_used = max_used;
+    plan->max_task_splits = max_task_splits;
+    plan->total_q_rows = static_cast<int>(rows);
+    plan->kv_tokens = kv_tokens;
+    plan->num_pages = num_pages;
+    plan->kv_indices = kv_indices;
+    plan->valid = true;
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *out,
+                     pgqa_dtype out_dtype, float *lse, float sm_scale, pgqa_stream_t stream) {
+    if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->valid) return fail(PGQA_ERR_INVALID_ARG, "run() before a successful plan_update()");
+    const pgqa_plan_config &c = plan->cfg;
+    if (out_dtype != PGQA_FP32 && out_dtype != c.dtype)
+        return fail(PGQA_ERR_UNSUPPORTED, "out_dtype must be fp32 or the plan's dtype");
+    if (plan->n_items == 0) return PGQA_OK;
+    if (!q || !k_pool || !v_pool || !out) return fail(PGQA_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PGQA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != plan->device) return fail(PGQA_ERR_INVALID_ARG, "plan belongs to device %d, current is %d", plan->device, dev);
+    unsigned int *flags = nullptr;
+    pgqa_status s = device_flags(&flags);
+    if (s != PGQA_OK) return s;
+    const CUtensorMap *mk = nullptr, *mv = nullptr;
+    s = pool_map(plan, k_pool, &mk);
+    if (s == PGQA_OK) s = pool_map(plan, v_pool, &mv);
+    if (s != PGQA_OK) return s;
+
+    const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(c.head_dim));
+    DecodeParams p{};
+    p.q = q;
+    p.items = plan->items();
+    p.kv_indices = plan->kv_indices;
+    p.num_pages = plan->num_pages;
+    p.page_size = c.page_size;
+    p.box_rows = plan->box_rows;
+    p.num_qo_heads = c.num_qo_heads;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.lse = lse;
+    p.partial_o = plan->d_partial_o;
+    p.partial_lse = plan->d_partial_lse;
+    p.flags = flags;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    e = launch_decode(c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items, true, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (plan->n_tasks > 0) {
+        MergeParams mp{};
+        mp.tasks = plan->tasks();
+        mp.partial_o = plan->d_partial_o;
+        mp.partial_lse = plan->d_partial_lse;
+        mp.out = out;
+        mp.out_dtype = out_dtype;
+        mp.lse = lse;
+        mp.num_qo_heads = c.num_qo_heads;
+        mp.group = plan->group;
+        mp.head_dim = c.head_dim;
+        e = launch_merge(mp, plan->n_tasks, plan->max_task_splits, true, st);
+        if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    }
+    return PGQA_OK;
+}
+
+}  // extern "C"

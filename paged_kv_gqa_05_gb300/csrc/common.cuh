@@ -1,0 +1,187 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through the runtime)
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedgqa.h"
+
+namespace pgqa {
+
+// ---------------------------------------------------------------------------
+// Work description produced by plan_update (host) and read by the kernels.
+// ---------------------------------------------------------------------------
+
+// One CTA of the split-KV partial kernel: one (query row, kv head, key slice).
+struct alignas(16) WorkItem {
+    int32_t page_base;  // kv_indptr[request]: first entry of the request's pages in kv_indices
+    int32_t tok_begin;  // key slice [tok_begin, tok_end), tok_begin a multiple of the warp tile
+    int32_t tok_end;    // <= the row's admissible key count
+    int32_t q_row;      // query row
+    int32_t kv_head;
+    int32_t out_slot;   // < 0: write the final output of (q_row, kv_head);
+                        // >= 0: write partial slot out_slot (merged later)
+    int32_t pad0, pad1;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+
+// One merge: the partial slots [slot_base, slot_base + num_splits) of (q_row, kv_head).
+struct alignas(16) MergeTask {
+    int32_t q_row;
+    int32_t kv_head;
+    int32_t slot_base;
+    int32_t num_splits;
+};
+static_assert(sizeof(MergeTask) == 16, "MergeTask is 16 bytes");
+
+// Warp tile (tokens one warp owns per pipeline stage) of the decode kernel.
+constexpr int decode_warp_tile(int head_dim) { return head_dim == 64 ? 32 : 16; }
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeStages = 3;
+
+struct DecodeParams {
+    const void *q;             // [rows, Hq, D]
+    const WorkItem *items;
+    const int32_t *kv_indices;
+    int64_t num_pages;
+    int page_size;
+    int box_rows;              // rows per TMA box: min(page_size, warp tile)
+    int num_qo_heads;
+    float scale_log2;          // sm_scale * log2(e)
+    void *out;                 // [rows, Hq, D] of out_dtype
+    int out_dtype;             // pgqa_dtype
+    float *lse;                // [rows, Hq] natural log, nullable
+    float *partial_o;          // [slots, G, D]
+    float *partial_lse;        // [slots, G] log2 domain
+    unsigned int *flags;       // device flag word
+};
+
+struct MergeParams {
+    const MergeTask *tasks;
+    const float *partial_o;    // [slots, G, D]
+    const float *partial_lse;  // [slots, G] log2 domain
+    void *out;
+    int out_dtype;
+    float *lse;
+    int num_qo_heads;
+    int group;                 // G
+    int head_dim;
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_decode(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items,
+                          bool pdl, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
+                         cudaStream_t stream);
+cudaError_t launch_kv_append(void *k_pool, void *v_pool, const void *k, const void *v,
+                             const int64_t *slot_mapping, int64_t num_tokens, int64_t num_slots,
+                             int row_bytes, unsigned int *flags, bool pdl, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Device helpers (inline PTX)
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the barrier phase with the given parity; gives up after ~2 s and
+// returns false (the caller raises PGQA_FLAG_WAIT_TIMEOUT instead of hanging).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 1023u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
+// 3-D tiled TMA load into CTA shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory, and let
+// the next grid start its prologue early.  No-ops without the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte shared-memory load through a plain C++ access, so the compiler orders
+// it against __syncwarp and the barrier waits (which clobber memory).
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// Two packed 16-bit floats -> two fp32 (exact widening).
+template <typename T>
+__device__ __forceinline__ float2 widen2(uint32_t packed);
+
+template <>
+__device__ __forceinline__ float2 widen2<__nv_bfloat16>(uint32_t packed) {
+    // bf16 is the upper half of an fp32: shift the low element up, mask the high one.
+    return make_float2(__uint_as_float(packed << 16), __uint_as_float(packed & 0xffff0000u));
+}
+
+template <>
+__device__ __forceinline__ float2 widen2<__half>(uint32_t packed) {
+    __half2 h = *reinterpret_cast<__half2 *>(&packed);
+    return __half22float2(h);
+}
+
+template <typename T>
+__device__ __forceinline__ T narrow(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half narrow<__half>(float x) { return __float2half_rn(x); }
+
+#endif  // __CUDACC__
+
+}  // namespace pgqa

@@ -1,0 +1,10 @@
+// Split-KV decode partial kernel instantiated for fp16, head_dim 64, groups 1..8.
+#include "decode.cuh"
+
+namespace pgqa {
+cudaError_t launch_decode_fp16_d64(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const DecodeParams &p, int num_items, bool pdl,
+                                      cudaStream_t stream) {
+    return launch_decode_dt<64, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
+}
+}  // namespace pgqa

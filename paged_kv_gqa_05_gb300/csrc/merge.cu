@@ -1,0 +1,149 @@
+// Log-sum-exp merge of split-KV partials.
+//
+// "A library kernel for decode", section "What changed": the partial results of
+// a request's slices are merged.  Each slice s of (query row, head) left an
+// output o_s normalised over its slice and lse_s (log2 domain); the merged
+// result is
+//     lse = log2 sum_s 2^lse_s,   o = sum_s 2^(lse_s - lse) o_s,
+// with empty slices (lse_s = -inf) carrying no weight.
+//
+// Grid: (merge task, head within the group, 32-channel chunk).  A block of 256
+// threads = 8 float4 columns x 32 slice groups, so a long list of slices is
+// read with many independent coalesced loads in flight.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace pgqa {
+
+namespace {
+
+constexpr int kMergeThreads = 256;
+constexpr int kChunk = 32;  // channels per block
+
+__device__ __forceinline__ float block_reduce(float v, float *scratch, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, m);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = scratch[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
+    return v;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void put(void *out, size_t i, float v);
+template <>
+__device__ __forceinline__ void put<float>(void *out, size_t i, float v) { static_cast<float *>(out)[i] = v; }
+template <>
+__device__ __forceinline__ void put<__nv_bfloat16>(void *out, size_t i, float v) {
+    static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ void put<__half>(void *out, size_t i, float v) {
+    static_cast<__half *>(out)[i] = __float2half_rn(v);
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+    extern __shared__ float sm[];
+    float *red = sm;                         // [32 slice groups][32 channels]
+    float *scratch = red + 32 * kChunk;      // [8]
+    float *w = scratch + 8;                  // [num_splits]
+
+    const MergeTask t = p.tasks[blockIdx.x];  // written by plan_update's copy only
+    const int h = blockIdx.y;
+    const int c0 = blockIdx.z * kChunk;
+    const int G = p.group, D = p.head_dim, ns = t.num_splits;
+
+    pdl_wait();
+
+    const float *lse_in = p.partial_lse + static_cast<size_t>(t.slot_base) * G + h;
+    float mx = -INFINITY;
+    for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+        const float v = lse_in[static_cast<size_t>(s) * G];
+        w[s] = v;
+        mx = fmaxf(mx, v);
+    }
+    mx = block_reduce(mx, scratch, true);
+    float sum = 0.f;
+    for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+        const float e = (w[s] == -INFINITY) ? 0.f : exp2f(w[s] - mx);
+        w[s] = e;
+        sum += e;
+    }
+    sum = block_reduce(sum, scratch, false);  // also publishes w[] to the block
+
+    const int c4 = threadIdx.x & 7, sg = threadIdx.x >> 3;
+    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + c0 + c4 * 4;
+    const size_t stride = static_cast<size_t>(G) * D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = sg; s < ns; s += 32) {
+        const float ws = w[s];
+        if (ws != 0.f) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
+            acc.x += ws * v.x;
+            acc.y += ws * v.y;
+            acc.z += ws * v.z;
+            acc.w += ws * v.w;
+        }
+    }
+    reinterpret_cast<float4 *>(red)[sg * 8 + c4] = acc;
+    __syncthreads();
+    pdl_launch_dependents();
+    if (threadIdx.x < kChunk) {
+        float tot = 0.f;
+#pragma unroll 8
+        for (int g = 0; g < 32; ++g) tot += red[g * kChunk + threadIdx.x];
+        const int head = t.kv_head * G + h;
+        const size_t oi = (static_cast<size_t>(t.q_row) * p.num_qo_heads + head) * D + c0 + threadIdx.x;
+        put<OutT>(p.out, oi, sum > 0.f ? tot / sum : 0.f);
+        if (threadIdx.x == 0 && blockIdx.z == 0 && p.lse != nullptr)
+            p.lse[static_cast<size_t>(t.q_row) * p.num_qo_heads + head] =
+                sum > 0.f ? (mx + log2f(sum)) * 0.6931471805599453f : -INFINITY;
+    }
+}
+
+template <typename OutT>
+cudaError_t launch_merge_t(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
+                           cudaStream_t stream) {
+    const size_t smem = (32 * kChunk + 8 + static_cast<size_t>(max_splits)) * sizeof(float);
+    auto kern = merge_kernel<OutT>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_tasks, p.group, p.head_dim / kChunk);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
+                         cudaStream_t stream) {
+    switch (p.out_dtype) {
+        case PGQA_FP32: return launch_merge_t<float>(p, num_tasks, max_splits, pdl, stream);
+        case PGQA_BF16: return launch_merge_t<__nv_bfloat16>(p, num_tasks, max_splits, pdl, stream);
+        case PGQA_FP16: return launch_merge_t<__half>(p, num_tasks, max_splits, pdl, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pgqa

@@ -1,0 +1,68 @@
+"""GPU parity over the supported shape space on small seeded cases: every page
+size, both head dims, every group width, both 16-bit types, with kv lengths
+that leave ragged tails inside tiles and pages, empty requests, and forced
+splits."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_gqa_05_gb300 import workloads as W
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+LENS = [0, 1, 5, 16, 17, 31, 33, 100, 257, 700]
+
+
+@pytest.mark.parametrize("page_size,head_dim", list(itertools.product([16, 32, 64, 128, 256], [64, 128])))
+def test_page_sizes(page_size, head_dim):
+    w = W.custom("sweep", LENS, page_size, 14, 2, head_dim, "bf16", 256, seed=page_size + head_dim)
+    ro, rl = H.oracle_outputs(w)
+    for opts in ({}, {"split_tokens": 32}, {"max_splits": 1}):
+        out, lse, _ = H.gpu_outputs(w, **opts)
+        H.compare(out, lse, ro, rl, f"ps{page_size}/d{head_dim}/{opts}")
+
+
+@pytest.mark.parametrize("group,dtype,head_dim",
+                         list(itertools.product([1, 2, 3, 4, 5, 6, 7, 8], ["bf16", "fp16"], [64, 128])))
+def test_groups(group, dtype, head_dim):
+    hkv = 2 if group <= 4 else 1
+    w = W.custom("grp", [3, 40, 129, 300], 16, group * hkv, hkv, head_dim, dtype, 64,
+                 seed=group * 7 + head_dim)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64)
+    H.compare(out, lse, ro, rl, f"g{group}/{dtype}/d{head_dim}")
+
+
+def test_all_empty_batch():
+    w = W.custom("empty", [0, 0, 0], 16, 4, 2, 64, "bf16", 4, seed=1)
+    out, lse, _ = H.gpu_outputs(w)
+    assert not out.any() and np.all(lse == -np.inf)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_multi_row_requests(causal):
+    """Ragged rows (qo_indptr) with and without the bottom-right causal mask."""
+    w = W.custom("rag", [40, 7, 300, 64], 16, 14, 2, 64, "bf16", 64, seed=11,
+                 qo_lens=[13, 1, 5, 64], causal=causal)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64)
+    H.compare(out, lse, ro, rl, f"ragged causal={causal}")
+
+
+def test_explicit_scale():
+    import oracle
+    import paged_kv_gqa_05_gb300 as pg
+    w = W.custom("scale", [50, 77], 16, 8, 2, 128, "fp16", 32, seed=3)
+    ro, rl = oracle.get().paged_attention(W.raw16(w.q), W.raw16(w.k_pool), W.raw16(w.v_pool),
+                                          w.kv_indptr, w.kv_indices, w.last_page_len, "fp16",
+                                          scale=0.3)
+    dev = H.to_device(w)
+    plan = pg.Plan(8, 2, 128, 16, torch.float16, 2, 2)
+    plan.update(w.kv_indptr, w.last_page_len, dev["kv_indices"], w.num_pages)
+    lse = torch.empty(2, 8, device="cuda")
+    out = plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out_dtype=torch.float32, lse=lse,
+                   sm_scale=0.3)
+    H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "scale 0.3")
