@@ -227,7 +227,7 @@ def run_ours(args, rank, world, local):
     dt = L["q"][0].dtype
     plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dt, max_batch=w.batch,
                    max_q_rows=w.rows, max_splits=args.max_splits, split_tokens=args.split_tokens,
-                   ctas_per_sm=args.ctas_per_sm)
+                   ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel)
     stream = torch.cuda.Stream(device)
     launches_per_layer = {}
 
@@ -342,6 +342,7 @@ def run_ours(args, rank, world, local):
             "kv_tokens": int(w.kv_lens.sum()),
             "l2": f"inputs larger than L2: {layers} independent layer pools per step",
             "graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single",
+            "decode_kernel": args.decode_kernel,
             "plan": {k: info[k] for k in ("num_items", "num_merge_tasks", "split_tokens", "max_splits_used",
                                           "num_sms")},
         },
@@ -466,6 +467,7 @@ def main(argv=None):
     ap.add_argument("--split-tokens", type=int, default=0)
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

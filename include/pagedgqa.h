@@ -63,6 +63,7 @@ typedef enum pgqa_dtype { PGQA_BF16 = 0, PGQA_FP16 = 1, PGQA_FP32 = 2 } pgqa_dty
 #define PGQA_FLAG_PAGE_INDEX 1u   /* a page index >= num_pages was skipped */
 #define PGQA_FLAG_SLOT_RANGE 2u   /* an append slot >= num_pages * page_size was skipped */
 #define PGQA_FLAG_WAIT_TIMEOUT 4u /* a pipeline barrier wait gave up (bounded spin) */
+#define PGQA_FLAG_SMEM_ALIGN 8u   /* shared memory too coarsely aligned for the TMA layout; CTA skipped */
 
 PGQA_API int pgqa_abi_version(void);
 PGQA_API const char *pgqa_status_string(pgqa_status status);
@@ -120,7 +121,13 @@ typedef struct pgqa_plan_config {
     int split_tokens;     /* > 0 forces this slice length (rounded up to the kernel tile);
                              0 = choose it so that the slices fill the SMs */
     int ctas_per_sm;      /* occupancy target of the split heuristic; 0 = library default */
+    int decode_kernel;    /* PGQA_DECODE_AUTO (tensor cores), PGQA_DECODE_TENSOR_CORE or
+                             PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
 } pgqa_plan_config;
+
+#define PGQA_DECODE_AUTO 0
+#define PGQA_DECODE_TENSOR_CORE 1
+#define PGQA_DECODE_CUDA_CORE 2
 
 /*
  * Creates a plan on the current device.  Allocates its device and pinned host

@@ -14,19 +14,19 @@
 #include "common.cuh"
 
 namespace pgqa {
-cudaError_t launch_decode_bf16_d64(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d128(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d64(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d128(int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+using DecodeLauncher = cudaError_t (*)(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &,
+                                        int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
 
-cudaError_t launch_decode(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
                           cudaStream_t stream) {
-    if (dtype == PGQA_BF16)
-        return head_dim == 64 ? launch_decode_bf16_d64(group, tm_k, tm_v, p, num_items, pdl, stream)
-                              : launch_decode_bf16_d128(group, tm_k, tm_v, p, num_items, pdl, stream);
-    return head_dim == 64 ? launch_decode_fp16_d64(group, tm_k, tm_v, p, num_items, pdl, stream)
-                          : launch_decode_fp16_d128(group, tm_k, tm_v, p, num_items, pdl, stream);
+    DecodeLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_decode_bf16_d64 : launch_decode_bf16_d128)
+                                          : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
+    return f(kind, group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa
 
@@ -92,18 +92,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // The pool [num_pages, page_size, Hkv, D] as the 3-D tensor {D, Hkv, rows};
 // one box is `box_rows` consecutive rows of one kv head.
 static pgqa_status make_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages, int page_size,
-                                 int num_kv_heads, int head_dim, pgqa_dtype dt, int box_rows) {
+                                 int num_kv_heads, int head_dim, pgqa_dtype dt, int box_rows, bool swizzle128) {
     auto fn = encode_fn();
     if (!fn) return fail(PGQA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_kv_heads),
                                 static_cast<cuuint64_t>(num_pages) * page_size};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
                                    static_cast<cuuint64_t>(num_kv_heads) * head_dim * 2};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1u, static_cast<cuuint32_t>(box_rows)};
+    // The tensor-core kernel takes 64-channel (128-byte) boxes with 128-byte swizzle; the
+    // CUDA-core kernel takes whole rows unswizzled.
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(swizzle128 ? 64 : head_dim), 1u,
+                               static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = fn(map, dt == PGQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     3, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return PGQA_OK;
@@ -138,6 +142,7 @@ struct pgqa_plan {
     int tile = 0;       // decode warp tile (tokens)
     int box_rows = 0;
     int ctas_per_sm = 0;
+    int kernel = PGQA_DECODE_TENSOR_CORE;
     int max_items = 0;  // capacity of the work list and of the partial slots
     int max_tasks = 0;
 
@@ -174,7 +179,8 @@ static pgqa_status pool_map(pgqa_plan *plan, const void *pool, const CUtensorMap
     MapCacheEntry &e = plan->maps[plan->map_next];
     plan->map_next = (plan->map_next + 1) % pgqa_plan::kMapCache;
     pgqa_status s = make_pool_map(&e.map, pool, plan->num_pages, plan->cfg.page_size, plan->cfg.num_kv_heads,
-                                  plan->cfg.head_dim, plan->cfg.dtype, plan->box_rows);
+                                  plan->cfg.head_dim, plan->cfg.dtype, plan->box_rows,
+                                  plan->kernel == PGQA_DECODE_TENSOR_CORE);
     if (s != PGQA_OK) {
         e.ptr = nullptr;
         return s;
@@ -275,6 +281,8 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "max_batch/max_q_rows out of range");
     if (c.max_splits < 0 || c.split_tokens < 0 || c.ctas_per_sm < 0)
         return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
+    if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
+        return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
 
     pgqa_plan *p = new (std::nothrow) pgqa_plan();
     if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
@@ -283,6 +291,7 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->tile = decode_warp_tile(c.head_dim);
     p->box_rows = std::min(c.page_size, p->tile);
     p->ctas_per_sm = c.ctas_per_sm > 0 ? c.ctas_per_sm : 2;
+    p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) {
@@ -518,7 +527,7 @@ pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const v
     p.partial_lse = plan->d_partial_lse;
     p.flags = flags;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_decode(c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items, true, st);
+    e = launch_decode(plan->kernel, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (plan->n_tasks > 0) {
         MergeParams mp{};

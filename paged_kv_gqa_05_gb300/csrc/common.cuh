@@ -72,7 +72,7 @@ struct MergeParams {
 };
 
 // Launchers (defined in the kernel translation units).
-cudaError_t launch_decode(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items,
                           bool pdl, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,

@@ -86,6 +86,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 
     // The work list is written by plan_update's copy, never by a kernel, so it
     // may be read before the programmatic-dependency wait.
+    if (smem_addr(smem) & 127u) {  // the stage layout assumes this alignment of the window
+        if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
+        return;
+    }
     const WorkItem it = p.items[blockIdx.x];
     const int ntiles = (it.tok_end - it.tok_begin + C::TW - 1) / C::TW;
     const int my_tiles = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
@@ -332,8 +336,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                 }
             }
         }
-        const float o = L > 0.f ? O / L : 0.f;
-        const float lse2 = L > 0.f ? M + log2f(L) : -INFINITY;
+        // L == 0 only for a slice with no admissible key; NaN (a poisoned row) propagates.
+        const float o = L == 0.f ? 0.f : O / L;
+        const float lse2 = L == 0.f ? -INFINITY : M + log2f(L);
         const int head = it.kv_head * G + h;
         if (it.out_slot < 0) {
             const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c;

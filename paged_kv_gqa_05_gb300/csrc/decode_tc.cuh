@@ -1,0 +1,442 @@
+// Split-KV paged GQA decode, tensor-core partial kernel (mma.sync m16n8k16).
+//
+// Same work decomposition as the CUDA-core kernel: one CTA per (query row, kv
+// head, key slice), serving the G <= 8 query heads that share the kv head, so
+// every K/V row of the slice is read from HBM once for the whole group
+// ("A library kernel for decode", section "What changed", for the split-KV
+// scheme; the "flashlet" README's NHD pool layout for the addressing).
+//
+// The group is a dense tile in "swap-AB" form: tokens are the M dimension (16
+// per MMA), the G heads padded to 8 are N, head_dim is K.
+//   S^T[16 tok x 8 heads]  = K[16 tok x d]   . Q^T[d x 8 heads]     (fp32 accumulate)
+//   O^T[16 d   x 8 heads] += V^T[16 d x tok] . P^T[tok x 8 heads]
+// K comes from shared memory through ldmatrix, V through ldmatrix.trans; Q^T
+// fragments are loaded once per CTA.  The probabilities leave the score
+// accumulator as (row = token, col = head) pairs; movmatrix.trans turns them into
+// the (row = token, col = head) B fragment of the second product.  P is carried
+// as two 16-bit terms (P = P_hi + P_lo, each rounded to the input type), so the
+// PV product keeps ~16 significant bits instead of 8 for bf16.
+//
+// Data movement: per-warp kDecodeStages-deep rings of shared-memory stages,
+// filled by 3-D TMA boxes with 128-byte swizzle ([rows, 1 kv head, 64 channels];
+// two boxes per row group when head_dim is 128), resolved through the page table
+// by lane 0 and completed on per-stage mbarriers.  The swizzle makes every
+// ldmatrix phase touch eight different 16-byte bank groups.
+#pragma once
+
+#include <math.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace pgqa {
+
+template <typename T>
+struct MmaType;
+template <>
+struct MmaType<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+template <>
+struct MmaType<__half> {
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// 16-bit value of the packed pair -> fp32 (bf16: upper bits of an fp32).
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t v) { return widen2<T>(v); }
+
+template <int D>
+struct TcCfg {
+    static constexpr int TW = decode_warp_tile(D);      // tokens per warp tile (32 for d64, 16 for d128)
+    static constexpr int MT = TW / 16;                   // token m-tiles per warp tile
+    static constexpr int HALVES = D / 64;                // 128-byte (64-channel) column blocks per row
+    static constexpr int NW = kDecodeWarps;
+    static constexpr int ST = kDecodeStages;
+    static constexpr int HALF_BYTES = TW * 128;          // one 64-channel block of a tile
+    static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K tile, then V tile
+    static constexpr int PIPE_BYTES = NW * ST * STAGE_BYTES;
+    static constexpr int BAR_BYTES = NW * ST * 8;
+    static constexpr int DT = D / 16;                    // d m-tiles of the PV product
+    static constexpr int KS = D / 16;                    // k-steps of the QK product
+    static constexpr int COMBINE_BYTES = NW * 8 * (D + 2) * 4;
+    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES;
+    static_assert(COMBINE_BYTES <= PIPE_BYTES, "combine buffer reuses the stages");
+    static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
+};
+
+// Byte offset of 16-byte chunk `c` (0..D/8-1) of tile row `r` inside a stage's
+// K or V tile, as the 128B-swizzled TMA boxes lay it out.
+template <int D>
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+    return (c >> 3) * TcCfg<D>::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DecodeParams p, int G) {
+    using C = TcCfg<D>;
+    using M = MmaType<T>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g8 = lane >> 2;  // fragment row group
+    const int c4 = lane & 3;   // fragment column pair
+
+    uint8_t *pipe = smem;
+    const uint32_t bar0 = smem_addr(smem + C::PIPE_BYTES) + warp * C::ST * 8;
+
+    if (smem_addr(smem) & 1023u) {  // the stage layout assumes this alignment of the window
+        if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
+        return;
+    }
+    const WorkItem it = p.items[blockIdx.x];  // written by plan_update's copy only
+    const int ntiles = (it.tok_end - it.tok_begin + C::TW - 1) / C::TW;
+    const int my_tiles = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < C::ST; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_barrier_init();
+        if (warp == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+    }
+    __syncwarp();
+
+    pdl_wait();
+
+    auto issue = [&](int k) {
+        const int tile = warp + k * C::NW;
+        const int t0 = it.tok_begin + tile * C::TW;
+        const int s = k % C::ST;
+        const uint32_t kdst = smem_addr(pipe + (warp * C::ST + s) * C::STAGE_BYTES);
+        const uint32_t vdst = kdst + C::TILE_BYTES;
+        const uint32_t bar = bar0 + 8 * s;
+        constexpr int MAXC = C::TW / 16;
+        int rows[MAXC];
+        int nvalid = 0;
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+            rows[c] = -1;
+            const int tt = t0 + c * p.box_rows;
+            if (c * p.box_rows < C::TW && tt < it.tok_end) {
+                const int64_t page = p.kv_indices[it.page_base + tt / p.page_size];
+                if (page < 0 || page >= p.num_pages) {
+                    atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
+                } else {
+                    rows[c] = static_cast<int>(page * p.page_size + tt % p.page_size);
+                    ++nvalid;
+                }
+            }
+        }
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid * p.box_rows * D * 2 * 2));
+#pragma unroll
+        for (int c = 0; c < MAXC; ++c) {
+            if (rows[c] >= 0) {
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf) {
+                    const uint32_t off = hf * C::HALF_BYTES + c * p.box_rows * 128;
+                    tma_load_3d(kdst + off, &tm_k, hf * 64, it.kv_head, rows[c], bar);
+                    tma_load_3d(vdst + off, &tm_v, hf * 64, it.kv_head, rows[c], bar);
+                }
+            }
+        }
+    };
+
+    if (lane == 0) {
+        const int pre = my_tiles < C::ST ? my_tiles : C::ST;
+        for (int k = 0; k < pre; ++k) issue(k);
+    }
+
+    // Q^T fragments (B operand): b0 = q[head g8][16ks + 2c4, +1], b1 = same + 8.
+    // Heads >= G are zero columns.
+    uint32_t qf[C::KS][2];
+    {
+        const bool real = g8 < G;
+        const T *qp = static_cast<const T *>(p.q) +
+                      (static_cast<size_t>(it.q_row) * p.num_qo_heads + it.kv_head * G + (real ? g8 : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(qp + ks * 16 + 2 * c4);
+            qf[ks][0] = real ? __ldg(w) : 0u;
+            qf[ks][1] = real ? __ldg(w + 4) : 0u;
+        }
+    }
+
+    // Running state for this thread's two head columns h0 = 2c4, h0 + 1.
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[C::DT][4];
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+
+    // ldmatrix lane roles: which 8x8 matrix this lane addresses and which row of it.
+    const int lm = lane >> 3, lr = lane & 7;
+
+    int waited = 0;
+    bool ok = true;
+    for (int k = 0; k < my_tiles; ++k) {
+        const int s = k % C::ST;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, (k / C::ST) & 1))) {
+            if (lane == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+            ok = false;
+            break;
+        }
+        waited = k + 1;
+        const int tile = warp + k * C::NW;
+        const int tb = it.tok_begin + tile * C::TW;
+        const int nvalid = min(C::TW, it.tok_end - tb);
+        const uint32_t kb = smem_addr(pipe + (warp * C::ST + s) * C::STAGE_BYTES);
+        const uint32_t vb = kb + C::TILE_BYTES;
+
+        // ---- S^T = K . Q^T for the tile's m-tiles (rows = tokens)
+        float sc[C::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                // matrices: 0 = (tok 0-7, chunk 2ks), 1 = (tok 8-15, 2ks), 2 = (tok 0-7, 2ks+1), 3 = (tok 8-15, 2ks+1)
+                const int r = mt * 16 + (lm & 1) * 8 + lr;
+                const int c = 2 * ks + (lm >> 1);
+                uint32_t a[4];
+                ldsm_x4(a, kb + tile_off<D>(r, c));
+                M::mma(sc[mt], a, qf[ks][0], qf[ks][1]);
+            }
+        }
+        // ---- mask, scale to log2 units, tile max per head column
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int tok = mt * 16 + g8 + (j >> 1) * 8;
+                const float x = tok < nvalid ? sc[mt][j] * p.scale_log2 : -INFINITY;
+                sc[mt][j] = x;
+                mx[j & 1] = fmaxf(mx[j & 1], x);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
+        }
+        float alpha[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float mn = fmaxf(m_run[h], mx[h]);
+            alpha[h] = (mn == m_run[h]) ? 1.f : exp2f(m_run[h] - mn);
+            m_run[h] = mn;
+            l_run[h] *= alpha[h];
+        }
+        if (alpha[0] != 1.f || alpha[1] != 1.f) {
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt) {
+                o[dt][0] *= alpha[0];
+                o[dt][1] *= alpha[1];
+                o[dt][2] *= alpha[0];
+                o[dt][3] *= alpha[1];
+            }
+        }
+        // ---- P = exp2(S - m); P^T fragments as hi + lo 16-bit terms
+        uint32_t pb_hi[C::MT][2], pb_lo[C::MT][2];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            float pr[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float x = sc[mt][j];
+                pr[j] = (x == -INFINITY) ? 0.f : exp2f(x - m_run[j & 1]);
+                l_run[j & 1] += pr[j];
+            }
+            // rows g8 (j = 0, 1) and g8 + 8 (j = 2, 3); columns 2c4, 2c4 + 1
+            const uint32_t h01 = M::pack(pr[0], pr[1]);
+            const uint32_t h23 = M::pack(pr[2], pr[3]);
+            const float2 f01 = unpack2<T>(h01), f23 = unpack2<T>(h23);
+            const uint32_t l01 = M::pack(pr[0] - f01.x, pr[1] - f01.y);
+            const uint32_t l23 = M::pack(pr[2] - f23.x, pr[3] - f23.y);
+            pb_hi[mt][0] = movm_t(h01);
+            pb_hi[mt][1] = movm_t(h23);
+            pb_lo[mt][0] = movm_t(l01);
+            pb_lo[mt][1] = movm_t(l23);
+        }
+        // ---- O^T += V^T . P^T   (k = tokens of each m-tile)
+        const bool partial = nvalid < C::TW;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            // A fragment token pairs of this lane: regs 0/1 hold tokens 2c4, 2c4+1; regs 2/3 hold +8.
+            uint32_t keep01 = 0xffffffffu, keep89 = 0xffffffffu;
+            if (partial) {
+                const int t = mt * 16 + 2 * c4;
+                keep01 = (t < nvalid ? 0x0000ffffu : 0u) | (t + 1 < nvalid ? 0xffff0000u : 0u);
+                keep89 = (t + 8 < nvalid ? 0x0000ffffu : 0u) | (t + 9 < nvalid ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt) {
+                // matrices: 0 = (tok 0-7, chunk 2dt), 1 = (tok 0-7, 2dt+1), 2 = (tok 8-15, 2dt), 3 = (tok 8-15, 2dt+1)
+                const int r = mt * 16 + (lm >> 1) * 8 + lr;
+                const int c = 2 * dt + (lm & 1);
+                uint32_t a[4];
+                ldsm_x4_t(a, vb + tile_off<D>(r, c));
+                if (partial) {  // rows past the slice may hold anything (NaN included): zero them
+                    a[0] &= keep01;
+                    a[1] &= keep01;
+                    a[2] &= keep89;
+                    a[3] &= keep89;
+                }
+                M::mma(o[dt], a, pb_hi[mt][0], pb_hi[mt][1]);
+                M::mma(o[dt], a, pb_lo[mt][0], pb_lo[mt][1]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && k + C::ST < my_tiles) issue(k + C::ST);
+    }
+
+    if (!ok && lane == 0) {
+        const int issued = my_tiles < waited + C::ST ? my_tiles : waited + C::ST;
+        for (int k = waited; k < issued; ++k) mbar_wait_bounded(bar0 + 8 * (k % C::ST), (k / C::ST) & 1);
+    }
+
+    pdl_launch_dependents();
+
+    // ---- combine the warps: per head column, (m, l, O)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+    }
+    __syncthreads();
+    float *cm = reinterpret_cast<float *>(smem);  // [NW][8]
+    float *cl = cm + C::NW * 8;                   // [NW][8]
+    float *co = cl + C::NW * 8;                   // [NW][8][D]
+    if (g8 == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            cm[warp * 8 + 2 * c4 + h] = m_run[h];
+            cl[warp * 8 + 2 * c4 + h] = l_run[h];
+        }
+    }
+#pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt) {
+        float *ow = co + warp * 8 * D;
+        ow[(2 * c4) * D + dt * 16 + g8] = o[dt][0];
+        ow[(2 * c4 + 1) * D + dt * 16 + g8] = o[dt][1];
+        ow[(2 * c4) * D + dt * 16 + g8 + 8] = o[dt][2];
+        ow[(2 * c4 + 1) * D + dt * 16 + g8 + 8] = o[dt][3];
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < G * D; idx += C::NW * 32) {
+        const int h = idx / D;
+        const int c = idx - h * D;
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NW; ++w) Mx = fmaxf(Mx, cm[w * 8 + h]);
+        float L = 0.f, O = 0.f;
+        if (Mx != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::NW; ++w) {
+                const float mw = cm[w * 8 + h];
+                if (mw != -INFINITY) {
+                    const float wt = exp2f(mw - Mx);
+                    L += cl[w * 8 + h] * wt;
+                    O += co[(w * 8 + h) * D + c] * wt;
+                }
+            }
+        }
+        // L == 0 only for a slice with no admissible key; NaN (a poisoned row) propagates.
+        const float ov = L == 0.f ? 0.f : O / L;
+        const float lse2 = L == 0.f ? -INFINITY : Mx + log2f(L);
+        const int head = it.kv_head * G + h;
+        if (it.out_slot < 0) {
+            const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c;
+            if (p.out_dtype == PGQA_FP32)
+                static_cast<float *>(p.out)[oi] = ov;
+            else
+                static_cast<T *>(p.out)[oi] = narrow<T>(ov);
+            if (c == 0 && p.lse != nullptr)
+                p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = lse2 * 0.6931471805599453f;
+        } else {
+            const size_t slot = static_cast<size_t>(it.out_slot) * G + h;
+            p.partial_o[slot * D + c] = ov;
+            if (c == 0) p.partial_lse[slot] = lse2;
+        }
+    }
+}
+
+template <int D, typename T>
+cudaError_t launch_decode_tc(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
+                             int num_items, bool pdl, cudaStream_t stream) {
+    using C = TcCfg<D>;
+    auto kern = decode_tc_kernel<D, T>;
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_items);
+    cfg.blockDim = dim3(C::NW * 32);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p, group);
+}
+
+}  // namespace pgqa

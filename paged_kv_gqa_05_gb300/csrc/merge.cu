@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     mx = block_reduce(mx, scratch, true);
     float sum = 0.f;
     for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
-        const float e = (w[s] == -INFINITY) ? 0.f : exp2f(w[s] - mx);
+        const float e = (w[s] == -INFINITY) ? 0.f : exp2f(w[s] - mx);  // NaN lse stays NaN
         w[s] = e;
         sum += e;
     }
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 #pragma unroll 4
     for (int s = sg; s < ns; s += 32) {
         const float ws = w[s];
-        if (ws != 0.f) {
+        if (ws != 0.f) {  // also taken for NaN weights
             const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
             acc.x += ws * v.x;
             acc.y += ws * v.y;
@@ -104,10 +104,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         for (int g = 0; g < 32; ++g) tot += red[g * kChunk + threadIdx.x];
         const int head = t.kv_head * G + h;
         const size_t oi = (static_cast<size_t>(t.q_row) * p.num_qo_heads + head) * D + c0 + threadIdx.x;
-        put<OutT>(p.out, oi, sum > 0.f ? tot / sum : 0.f);
+        put<OutT>(p.out, oi, sum == 0.f ? 0.f : tot / sum);  // NaN propagates
         if (threadIdx.x == 0 && blockIdx.z == 0 && p.lse != nullptr)
             p.lse[static_cast<size_t>(t.q_row) * p.num_qo_heads + head] =
-                sum > 0.f ? (mx + log2f(sum)) * 0.6931471805599453f : -INFINITY;
+                sum == 0.f ? -INFINITY : (mx + log2f(sum)) * 0.6931471805599453f;
     }
 }
 

@@ -31,6 +31,14 @@ def test_workload_fp32_out(name):
     assert mx < 1e-4, f"{name}: fp32 path error {mx:.2e} is larger than fp32 arithmetic explains"
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen05_decode", "qwen15_mixed", "long_context_b1", "ragged"])
+def test_workload_cuda_core_kernel(name):
+    """The CUDA-core (fp32 FMA) decode kernel on the same workloads."""
+    w, (ro, rl) = _ref(name)
+    out, lse, _ = H.gpu_outputs(w, torch.float32, decode_kernel="cuda_core")
+    H.compare(out, lse, ro, rl, name + "/cuda_core")
+
+
 @pytest.mark.parametrize("name", ["tiny", "qwen05_decode", "qwen15_mixed", "ragged"])
 def test_workload_native_out(name):
     w, (ro, rl) = _ref(name)

@@ -16,24 +16,29 @@ pytestmark = pytest.mark.gpu
 LENS = [0, 1, 5, 16, 17, 31, 33, 100, 257, 700]
 
 
+KERNELS = ["tensor_core", "cuda_core"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("page_size,head_dim", list(itertools.product([16, 32, 64, 128, 256], [64, 128])))
-def test_page_sizes(page_size, head_dim):
+def test_page_sizes(page_size, head_dim, kernel):
     w = W.custom("sweep", LENS, page_size, 14, 2, head_dim, "bf16", 256, seed=page_size + head_dim)
     ro, rl = H.oracle_outputs(w)
     for opts in ({}, {"split_tokens": 32}, {"max_splits": 1}):
-        out, lse, _ = H.gpu_outputs(w, **opts)
-        H.compare(out, lse, ro, rl, f"ps{page_size}/d{head_dim}/{opts}")
+        out, lse, _ = H.gpu_outputs(w, decode_kernel=kernel, **opts)
+        H.compare(out, lse, ro, rl, f"{kernel}/ps{page_size}/d{head_dim}/{opts}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("group,dtype,head_dim",
                          list(itertools.product([1, 2, 3, 4, 5, 6, 7, 8], ["bf16", "fp16"], [64, 128])))
-def test_groups(group, dtype, head_dim):
+def test_groups(group, dtype, head_dim, kernel):
     hkv = 2 if group <= 4 else 1
     w = W.custom("grp", [3, 40, 129, 300], 16, group * hkv, hkv, head_dim, dtype, 64,
                  seed=group * 7 + head_dim)
     ro, rl = H.oracle_outputs(w)
-    out, lse, _ = H.gpu_outputs(w, split_tokens=64)
-    H.compare(out, lse, ro, rl, f"g{group}/{dtype}/d{head_dim}")
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64, decode_kernel=kernel)
+    H.compare(out, lse, ro, rl, f"{kernel}/g{group}/{dtype}/d{head_dim}")
 
 
 def test_all_empty_batch():
@@ -42,13 +47,14 @@ def test_all_empty_batch():
     assert not out.any() and np.all(lse == -np.inf)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("causal", [True, False])
-def test_multi_row_requests(causal):
+def test_multi_row_requests(causal, kernel):
     """Ragged rows (qo_indptr) with and without the bottom-right causal mask."""
     w = W.custom("rag", [40, 7, 300, 64], 16, 14, 2, 64, "bf16", 64, seed=11,
                  qo_lens=[13, 1, 5, 64], causal=causal)
     ro, rl = H.oracle_outputs(w)
-    out, lse, _ = H.gpu_outputs(w, split_tokens=64)
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64, decode_kernel=kernel)
     H.compare(out, lse, ro, rl, f"ragged causal={causal}")
 
 
