@@ -235,8 +235,16 @@ def run_ours(args, rank, world, local):
         plan.update(w.kv_indptr, w.last_page_len, L["kv_indices"], w.num_pages, qo_indptr=w.qo_indptr,
                     causal=w.causal, stream=stream)
 
+    fused = args.append_mode == "fused" and L["slots"] is not None
+
     def layer_calls(with_append=True):
         for l in range(layers):
+            if fused and with_append:
+                # one launch: the step's new rows are appended and attended together; the
+                # pool rows it reads were written by earlier steps (no in-flight writer)
+                pg.append_run(plan.handle, L["k_new"][l], L["v_new"][l], L["q"][l], L["k_pool"][l],
+                              L["v_pool"][l], out=L["out"][l], pool_stable=True, stream=stream)
+                continue
             if with_append and L["slots"] is not None:
                 pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
                              stream=stream)
@@ -247,7 +255,8 @@ def run_ours(args, rank, world, local):
         layer_calls()  # eager warm-up: loads modules, sets kernel attributes, builds TMA maps
     torch.cuda.synchronize()
     info = plan.info()
-    per_layer_launches = (1 if L["slots"] is not None else 0) + 1 + (1 if info["num_merge_tasks"] else 0)
+    per_layer_launches = ((1 if (L["slots"] is not None and not fused) else 0) + 1 +
+                          (1 if info["num_merge_tasks"] else 0))
 
     graphs = {}
     if not args.no_graph:
@@ -342,7 +351,7 @@ def run_ours(args, rank, world, local):
             "kv_tokens": int(w.kv_lens.sum()),
             "l2": f"inputs larger than L2: {layers} independent layer pools per step",
             "graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single",
-            "decode_kernel": args.decode_kernel,
+            "decode_kernel": args.decode_kernel, "append_mode": args.append_mode if L["slots"] is not None else None,
             "plan": {k: info[k] for k in ("num_items", "num_merge_tasks", "split_tokens", "max_splits_used",
                                           "num_sms")},
         },
@@ -468,6 +477,8 @@ def main(argv=None):
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto")
+    ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
+                    help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

@@ -155,8 +155,11 @@ PGQA_API pgqa_status pgqa_plan_create(pgqa_plan **plan, const pgqa_plan_config *
  *                       owns rows qo_indptr[b] .. qo_indptr[b+1] (the ragged
  *                       form of the "flashlet" README, design bullets:
  *                       qo_indptr lengths [512, 1, 1, ...] in one call).
- *   kv_indices          [kv_indptr[batch]] int32, DEVICE; must stay valid and
- *                       unchanged until the last run() that uses this plan.
+ *   kv_indices          [kv_indptr[batch]] int32, DEVICE; its final contents must
+ *                       be in place (in stream order) when plan_update is called,
+ *                       and it must stay valid and unchanged until the last run()
+ *                       that uses this plan (the kernels read it before waiting
+ *                       on the preceding kernel).
  *   kv_indices_host     optional host mirror of kv_indices (NULL allowed).  When
  *                       given, every index is checked here against num_pages;
  *                       when not, the kernels skip out-of-range pages and raise
@@ -195,6 +198,36 @@ PGQA_API pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr_
 PGQA_API pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const void *v_pool,
                      void *out, pgqa_dtype out_dtype, float *lse, float sm_scale,
                      pgqa_stream_t stream);
+
+/*
+ * pgqa_append_run -- kv_append and run() of one decode (or prefill) step in one launch.
+ *
+ * The paged append of the "flashlet" README's design bullets (new tokens' rows
+ * copied into their slots), folded into the attention call that reads them:
+ * request b's last qo_len(b) key positions (qo_len = its query rows; 1 for pure
+ * decode) take their K/V rows from k_new / v_new rows qo_indptr[b] ..
+ * qo_indptr[b+1] (row b when the plan has no qo_indptr).  The kernel uses those
+ * rows directly for the attention and also stores them into their pool slots,
+ * which the page table must already cover (kv_len counts the new tokens).
+ * Other arguments and the result are those of pgqa_run.
+ *
+ *   k_new, v_new  [total_q_rows, num_kv_heads, head_dim], the plan's dtype
+ *   k_pool, v_pool  written (new rows only) and read
+ *   flags         0, or PGQA_RUN_POOL_STABLE: no kernel still running when this
+ *                 call's kernel starts writes any pool row this call reads
+ *                 (other than the new rows).  The K/V loads then begin before
+ *                 the kernel waits for its predecessor on the stream, hiding the
+ *                 memory latency behind that kernel's tail.  A kernel that wrote
+ *                 those rows and is the immediate predecessor voids the promise.
+ * Errors: as pgqa_run; PGQA_ERR_UNSUPPORTED for a plan created with
+ * PGQA_DECODE_CUDA_CORE; PGQA_ERR_INVALID_ARG when a request has more query
+ * rows than keys.
+ */
+#define PGQA_RUN_POOL_STABLE 1
+
+PGQA_API pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const void *v_new, const void *q,
+                                     void *k_pool, void *v_pool, void *out, pgqa_dtype out_dtype, float *lse,
+                                     float sm_scale, int flags, pgqa_stream_t stream);
 
 /* Frees the plan's buffers (synchronising with its last enqueued copy).  NULL is a no-op. */
 PGQA_API pgqa_status pgqa_plan_destroy(pgqa_plan *plan);

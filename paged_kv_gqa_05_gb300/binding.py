@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "PGQA_OK", 1: "PGQA_ERR_INVALID_ARG", 2: "PGQA_ERR_UNSUPPORTE
 # Every entry point include/pagedgqa.h declares.
 EXPORTS = ("pgqa_abi_version", "pgqa_status_string", "pgqa_last_error", "pgqa_read_device_flags",
            "pgqa_kv_append", "pgqa_plan_create", "pgqa_plan_update", "pgqa_run",
-           "pgqa_plan_destroy", "pgqa_plan_get_info")
+           "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run")
 
 
 class PagedGQAError(RuntimeError):
@@ -85,6 +85,9 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                                      ctypes.c_int64, ctypes.c_int, _vp]
     lib.pgqa_run.restype = ctypes.c_int
     lib.pgqa_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_float, _vp]
+    lib.pgqa_append_run.restype = ctypes.c_int
+    lib.pgqa_append_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_float,
+                                    ctypes.c_int, _vp]
     lib.pgqa_plan_destroy.restype = ctypes.c_int
     lib.pgqa_plan_destroy.argtypes = [_vp]
     lib.pgqa_plan_get_info.restype = ctypes.c_int
@@ -196,6 +199,31 @@ def run(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
     return out
 
 
+POOL_STABLE = 1
+
+
+def append_run(plan: int, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+               v_pool: torch.Tensor, out: Optional[torch.Tensor] = None,
+               out_dtype: Optional[torch.dtype] = None, lse: Optional[torch.Tensor] = None,
+               sm_scale: float = 0.0, pool_stable: bool = False, stream=None) -> torch.Tensor:
+    """pgqa_append_run: the step's new K/V rows (one per query row) are appended and
+    attended in one launch."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    for t, name in ((k_pool, "k_pool"), (v_pool, "v_pool"), (k_new, "k_new"), (v_new, "v_new")):
+        if t.dtype != q.dtype:
+            raise ValueError(f"{name} must have q's dtype")
+    if k_new.shape != v_new.shape or k_new.shape[0] != q.shape[0] or k_new.shape[1:] != k_pool.shape[2:]:
+        raise ValueError("k_new / v_new must be [q rows, num_kv_heads, head_dim]")
+    _check(load().pgqa_append_run(plan, _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(q, "q"),
+                                  _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dev(out, "out"),
+                                  TORCH_TO_CODE[out.dtype], None if lse is None else _dev(lse, "lse"),
+                                  float(sm_scale), POOL_STABLE if pool_stable else 0, _stream(stream)))
+    return out
+
+
 def plan_destroy(plan: int) -> None:
     _check(load().pgqa_plan_destroy(plan))
 
@@ -230,6 +258,9 @@ class Plan:
 
     def run(self, *args, **kwargs) -> torch.Tensor:
         return run(self.handle, *args, **kwargs)
+
+    def append_run(self, *args, **kwargs) -> torch.Tensor:
+        return append_run(self.handle, *args, **kwargs)
 
     def info(self) -> dict:
         return plan_get_info(self.handle)

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -157,6 +158,7 @@ struct pgqa_plan {
     bool valid = false;
     int n_items = 0, n_tasks = 0, split_tokens = 0, max_splits_used = 0, total_q_rows = 0;
     int max_task_splits = 0;
+    bool fusable = false;  // every request has at least as many keys as query rows
     int64_t kv_tokens = 0, num_pages = 0;
     const int32_t *kv_indices = nullptr;
 
@@ -385,21 +387,28 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
 
     // Admissible keys per query row (bottom-right causal for multi-row requests).
     struct Row {
-        int32_t q_row, page_base, n;
+        int32_t q_row, page_base, n;   // n: admissible keys of the row
+        int32_t new_begin, new_row_base, own_pos;
     };
     std::vector<Row> rowv;
     rowv.reserve(static_cast<size_t>(rows));
     int64_t work = 0, kv_tokens = 0;
+    bool fusable = true;
     for (int b = 0; b < batch; ++b) {
         const int64_t np = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
         const int64_t n = np == 0 ? 0 : (np - 1) * c.page_size + last_page_len[b];
         kv_tokens += n;
         const int64_t r0 = qo_indptr ? qo_indptr[b] : b, r1 = qo_indptr ? qo_indptr[b + 1] : b + 1;
         const int64_t L = r1 - r0;
+        // A fused append writes the request's last L key positions from the L new rows.
+        if (L > n) fusable = false;
+        const int64_t nb = L <= n ? n - L : INT32_MAX;
         for (int64_t r = r0; r < r1; ++r) {
             int64_t a = n;
             if (causal) a = std::min<int64_t>(n, std::max<int64_t>(0, n - L + (r - r0) + 1));
-            rowv.push_back({static_cast<int32_t>(r), kv_indptr[b], static_cast<int32_t>(a)});
+            rowv.push_back({static_cast<int32_t>(r), kv_indptr[b], static_cast<int32_t>(a),
+                            static_cast<int32_t>(nb), static_cast<int32_t>(L <= n ? r0 - nb : 0),
+                            static_cast<int32_t>(L <= n ? nb + (r - r0) : -1)});
             work += a;
         }
     }
@@ -410,8 +419,15 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     const int tile = plan->tile;
     const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
     int64_t ls;
+    const int64_t pairs = static_cast<int64_t>(rowv.size()) * c.num_kv_heads;
+    int64_t longest = 0;
+    for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
     if (c.split_tokens > 0) {
         ls = round_up(c.split_tokens, tile);
+    } else if (pairs >= plan->num_sms) {
+        // Every SM already has a (row, kv head) of its own: a split would only add
+        // per-CTA set-up and a merge.
+        ls = std::max<int64_t>(min_split, round_up(std::max<int64_t>(1, longest), tile));
     } else {
         const int64_t target = static_cast<int64_t>(plan->num_sms) * plan->ctas_per_sm;
         ls = std::max<int64_t>(min_split, round_up(std::max<int64_t>(1, ceil_div(work, target)), tile));
@@ -429,7 +445,8 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
             const int64_t len = n == 0 ? 0 : round_up(ceil_div(n, ns), tile);
             ns = n == 0 ? 1 : ceil_div(n, len);
             if (ns == 1) {
-                items.push_back({rw.page_base, 0, static_cast<int32_t>(n), rw.q_row, kvh, -1, 0, 0});
+                items.push_back({rw.page_base, 0, static_cast<int32_t>(n), rw.q_row, kvh, -1, rw.new_begin,
+                                 rw.new_row_base, rw.own_pos, 0, 0, 0});
                 continue;
             }
             if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_items)
@@ -437,7 +454,8 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
             for (int64_t s = 0; s < ns; ++s)
                 items.push_back({rw.page_base, static_cast<int32_t>(s * len),
                                  static_cast<int32_t>(std::min<int64_t>(n, (s + 1) * len)), rw.q_row, kvh,
-                                 slot + static_cast<int32_t>(s), 0, 0});
+                                 slot + static_cast<int32_t>(s), rw.new_begin, rw.new_row_base,
+                                 s == ns - 1 ? rw.own_pos : -1, 0, 0, 0});
             tasks.push_back({rw.q_row, kvh, slot, static_cast<int32_t>(ns)});
             slot += static_cast<int>(ns);
             max_used = std::max<int>(max_used, static_cast<int>(ns));
@@ -483,17 +501,32 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     plan->kv_tokens = kv_tokens;
     plan->num_pages = num_pages;
     plan->kv_indices = kv_indices;
+    plan->fusable = fusable;
     plan->valid = true;
     return PGQA_OK;
 }
 
-pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *out,
-                     pgqa_dtype out_dtype, float *lse, float sm_scale, pgqa_stream_t stream) {
+static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_new, const void *q, void *k_pool,
+                            void *v_pool, void *out, pgqa_dtype out_dtype, float *lse, float sm_scale, int flags,
+                            pgqa_stream_t stream) {
     if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
     if (!plan->valid) return fail(PGQA_ERR_INVALID_ARG, "run() before a successful plan_update()");
     const pgqa_plan_config &c = plan->cfg;
     if (out_dtype != PGQA_FP32 && out_dtype != c.dtype)
         return fail(PGQA_ERR_UNSUPPORTED, "out_dtype must be fp32 or the plan's dtype");
+    if (flags & ~PGQA_RUN_POOL_STABLE) return fail(PGQA_ERR_INVALID_ARG, "unknown run flags 0x%x", flags);
+    const bool fused = k_new != nullptr || v_new != nullptr;
+    if (fused) {
+        if (!k_new || !v_new) return fail(PGQA_ERR_INVALID_ARG, "k_new and v_new go together");
+        if (plan->kernel != PGQA_DECODE_TENSOR_CORE)
+            return fail(PGQA_ERR_UNSUPPORTED, "the fused append runs on the tensor-core decode kernel");
+        if (!plan->fusable)
+            return fail(PGQA_ERR_INVALID_ARG, "a request has more query rows than keys: nothing to append them to");
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return fail(PGQA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    } else if (flags & PGQA_RUN_POOL_STABLE) {
+        return fail(PGQA_ERR_INVALID_ARG, "PGQA_RUN_POOL_STABLE applies to pgqa_append_run");
+    }
     if (plan->n_items == 0) return PGQA_OK;
     if (!q || !k_pool || !v_pool || !out) return fail(PGQA_ERR_INVALID_ARG, "NULL tensor");
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
@@ -502,8 +535,8 @@ pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const v
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev != plan->device) return fail(PGQA_ERR_INVALID_ARG, "plan belongs to device %d, current is %d", plan->device, dev);
-    unsigned int *flags = nullptr;
-    pgqa_status s = device_flags(&flags);
+    unsigned int *dflags = nullptr;
+    pgqa_status s = device_flags(&dflags);
     if (s != PGQA_OK) return s;
     const CUtensorMap *mk = nullptr, *mv = nullptr;
     s = pool_map(plan, k_pool, &mk);
@@ -525,7 +558,13 @@ pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const v
     p.lse = lse;
     p.partial_o = plan->d_partial_o;
     p.partial_lse = plan->d_partial_lse;
-    p.flags = flags;
+    p.flags = dflags;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_pool = k_pool;
+    p.v_pool = v_pool;
+    p.num_kv_heads = c.num_kv_heads;
+    p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     e = launch_decode(plan->kernel, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -544,6 +583,19 @@ pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const v
         if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     }
     return PGQA_OK;
+}
+
+pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const void *v_pool, void *out,
+                     pgqa_dtype out_dtype, float *lse, float sm_scale, pgqa_stream_t stream) {
+    return run_impl(plan, nullptr, nullptr, q, const_cast<void *>(k_pool), const_cast<void *>(v_pool), out,
+                    out_dtype, lse, sm_scale, 0, stream);
+}
+
+pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const void *v_new, const void *q, void *k_pool,
+                            void *v_pool, void *out, pgqa_dtype out_dtype, float *lse, float sm_scale, int flags,
+                            pgqa_stream_t stream) {
+    if (!k_new || !v_new) return fail(PGQA_ERR_INVALID_ARG, "k_new / v_new is NULL");
+    return run_impl(plan, k_new, v_new, q, k_pool, v_pool, out, out_dtype, lse, sm_scale, flags, stream);
 }
 
 }  // extern "C"

@@ -17,16 +17,20 @@ namespace pgqa {
 
 // One CTA of the split-KV partial kernel: one (query row, kv head, key slice).
 struct alignas(16) WorkItem {
-    int32_t page_base;  // kv_indptr[request]: first entry of the request's pages in kv_indices
-    int32_t tok_begin;  // key slice [tok_begin, tok_end), tok_begin a multiple of the warp tile
-    int32_t tok_end;    // <= the row's admissible key count
-    int32_t q_row;      // query row
+    int32_t page_base;     // kv_indptr[request]: first entry of the request's pages in kv_indices
+    int32_t tok_begin;     // key slice [tok_begin, tok_end), tok_begin a multiple of the warp tile
+    int32_t tok_end;       // <= the row's admissible key count
+    int32_t q_row;         // query row
     int32_t kv_head;
-    int32_t out_slot;   // < 0: write the final output of (q_row, kv_head);
-                        // >= 0: write partial slot out_slot (merged later)
-    int32_t pad0, pad1;
+    int32_t out_slot;      // < 0: write the final output of (q_row, kv_head);
+                           // >= 0: write partial slot out_slot (merged later)
+    int32_t new_begin;     // first key position of the request holding one of the call's new rows
+                           // (the request's last qo_len positions); INT32_MAX when it has none
+    int32_t new_row_base;  // the new row of key position p is k_new[p + new_row_base]
+    int32_t write_pos;     // key position whose new row this item stores into the pool, or -1
+    int32_t pad0, pad1, pad2;
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
 
 // One merge: the partial slots [slot_base, slot_base + num_splits) of (q_row, kv_head).
 struct alignas(16) MergeTask {
@@ -57,6 +61,15 @@ struct DecodeParams {
     float *partial_o;          // [slots, G, D]
     float *partial_lse;        // [slots, G] log2 domain
     unsigned int *flags;       // device flag word
+    // fused append (all null for a plain run): new rows [rows, Hkv, D], one per query
+    // row, and the pools as plain pointers for storing them
+    const void *k_new;
+    const void *v_new;
+    void *k_pool;
+    void *v_pool;
+    int num_kv_heads;
+    int prefetch_pool;         // 1: the pool rows (other than the new ones) are stable, so
+                               // K/V loads may start before the grid-dependency wait
 };
 
 struct MergeParams {
@@ -100,6 +113,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Makes barrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -111,14 +130,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// One bounded probe of the barrier phase; the thread may sleep up to ~10 us inside
+// it (suspend-time hint) instead of spinning, and wakes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(10000u)
         : "memory");
     return ok != 0;
 }
@@ -130,7 +151,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 1023u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+        if ((it & 15u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
     }
 }
 
@@ -142,6 +163,48 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// Same, with an L2 cache policy (K/V are streamed once per call: evict first).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 int c2, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Page indices of a key slice, staged in shared memory by the whole CTA in one
+// round trip so that TMA issue never waits on a dependent global load.
+constexpr int kSlicePageCap = 512;
+
+struct SlicePages {
+    const int32_t *smem;       // [min(count, kSlicePageCap)]
+    const int32_t *global;     // kv_indices + page_base
+    int first;                 // page number (within the request) of smem[0]
+    __device__ __forceinline__ int64_t operator()(int tok, int page_size) const {
+        const int i = tok / page_size - first;
+        return i < kSlicePageCap ? smem[i] : global[first + i];
+    }
+};
+
+__device__ __forceinline__ SlicePages stage_slice_pages(int32_t *buf, const int32_t *kv_indices, int page_base,
+                                                       int tok_begin, int tok_end, int page_size) {
+    SlicePages sp;
+    sp.first = tok_begin / page_size;
+    sp.global = kv_indices + page_base;
+    sp.smem = buf;
+    const int n = tok_end > tok_begin ? (tok_end - 1) / page_size - sp.first + 1 : 0;
+    const int m = n < kSlicePageCap ? n : kSlicePageCap;
+    for (int i = threadIdx.x; i < m; i += blockDim.x) buf[i] = __ldg(sp.global + sp.first + i);
+    return sp;  // caller synchronises the CTA before use
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

@@ -53,7 +53,7 @@ struct DecodeCfg {
     static constexpr int PB_BYTES = NW * PB_WARP;
     static constexpr int NG = NW * GPW;                 // softmax groups per CTA
     static constexpr int COMBINE_BYTES = NG * G * (D + 2) * 4;
-    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + PB_BYTES;
+    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + PB_BYTES + kSlicePageCap * 4;
     static_assert(COMBINE_BYTES <= PIPE_BYTES, "combine buffer reuses the pipeline stages");
     static_assert(TW % 16 == 0, "warp tile covers whole 16-row boxes");
 };
@@ -86,13 +86,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 
     // The work list is written by plan_update's copy, never by a kernel, so it
     // may be read before the programmatic-dependency wait.
+    pdl_launch_dependents();  // the next grid waits for our completion before touching our outputs
     if (smem_addr(smem) & 127u) {  // the stage layout assumes this alignment of the window
         if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
         return;
     }
+    // The work list and kv_indices are final once plan_update is enqueued, so they
+    // are read before the dependency wait; q and the pools only after it.
     const WorkItem it = p.items[blockIdx.x];
     const int ntiles = (it.tok_end - it.tok_begin + C::TW - 1) / C::TW;
     const int my_tiles = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
+    int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PIPE_BYTES + C::BAR_BYTES + C::PB_BYTES);
 
     if (lane == 0) {
         for (int s = 0; s < C::ST; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -102,7 +106,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             prefetch_tensormap(&tm_v);
         }
     }
-    __syncwarp();
+    const SlicePages pages =
+        stage_slice_pages(page_buf, p.kv_indices, it.page_base, it.tok_begin, it.tok_end, p.page_size);
+    __syncthreads();
 
     pdl_wait();
 
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             rows[c] = -1;
             const int tt = t0 + c * p.box_rows;
             if (c * p.box_rows < C::TW && tt < it.tok_end) {
-                const int64_t page = p.kv_indices[it.page_base + tt / p.page_size];
+                const int64_t page = pages(tt, p.page_size);
                 if (page < 0 || page >= p.num_pages) {
                     atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
                 } else {
@@ -285,8 +291,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         const int issued = my_tiles < waited + C::ST ? my_tiles : waited + C::ST;
         for (int k = waited; k < issued; ++k) mbar_wait_bounded(bar0 + 8 * (k % C::ST), (k / C::ST) & 1);
     }
-
-    pdl_launch_dependents();
 
     // ---- combine the CTA's softmax groups
     float l_tot[G];

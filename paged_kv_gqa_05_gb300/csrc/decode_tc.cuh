@@ -101,8 +101,8 @@ struct TcCfg {
     static constexpr int BAR_BYTES = NW * ST * 8;
     static constexpr int DT = D / 16;                    // d m-tiles of the PV product
     static constexpr int KS = D / 16;                    // k-steps of the QK product
-    static constexpr int COMBINE_BYTES = NW * 8 * (D + 2) * 4;
-    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES;
+    static constexpr int COMBINE_BYTES = (NW * 8 * 2 + 8 + NW * 8 * (D + 4)) * 4;
+    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4;
     static_assert(COMBINE_BYTES <= PIPE_BYTES, "combine buffer reuses the stages");
     static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
 };
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                      const DecodeParams p, int G) {
     using C = TcCfg<D>;
     using M = MmaType<T>;
+    constexpr int CH = D / 8;  // 16-byte chunks per row
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int warp = threadIdx.x >> 5;
@@ -129,14 +130,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 
     uint8_t *pipe = smem;
     const uint32_t bar0 = smem_addr(smem + C::PIPE_BYTES) + warp * C::ST * 8;
+    int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PIPE_BYTES + C::BAR_BYTES);
 
     if (smem_addr(smem) & 1023u) {  // the stage layout assumes this alignment of the window
         if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
+        pdl_wait();
         return;
     }
-    const WorkItem it = p.items[blockIdx.x];  // written by plan_update's copy only
+    // The work list and kv_indices are final once plan_update is enqueued (its
+    // copy sits between any earlier writer and this kernel), so they are read
+    // before the grid-dependency wait; q and the new rows only after it.
+    const WorkItem it = p.items[blockIdx.x];
     const int ntiles = (it.tok_end - it.tok_begin + C::TW - 1) / C::TW;
     const int my_tiles = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
+    const bool fused = p.k_new != nullptr;
 
     if (lane == 0) {
         for (int s = 0; s < C::ST; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -146,9 +153,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             prefetch_tensormap(&tm_v);
         }
     }
-    __syncwarp();
-
-    pdl_wait();
+    const SlicePages pages =
+        stage_slice_pages(page_buf, p.kv_indices, it.page_base, it.tok_begin, it.tok_end, p.page_size);
+    __syncthreads();
+    const uint64_t policy = l2_evict_first_policy();
 
     auto issue = [&](int k) {
         const int tile = warp + k * C::NW;
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             rows[c] = -1;
             const int tt = t0 + c * p.box_rows;
             if (c * p.box_rows < C::TW && tt < it.tok_end) {
-                const int64_t page = p.kv_indices[it.page_base + tt / p.page_size];
+                const int64_t page = pages(tt, p.page_size);
                 if (page < 0 || page >= p.num_pages) {
                     atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
                 } else {
@@ -181,17 +189,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf) {
                     const uint32_t off = hf * C::HALF_BYTES + c * p.box_rows * 128;
-                    tma_load_3d(kdst + off, &tm_k, hf * 64, it.kv_head, rows[c], bar);
-                    tma_load_3d(vdst + off, &tm_v, hf * 64, it.kv_head, rows[c], bar);
+                    tma_load_3d_hint(kdst + off, &tm_k, hf * 64, it.kv_head, rows[c], bar, policy);
+                    tma_load_3d_hint(vdst + off, &tm_v, hf * 64, it.kv_head, rows[c], bar, policy);
                 }
             }
         }
     };
 
-    if (lane == 0) {
-        const int pre = my_tiles < C::ST ? my_tiles : C::ST;
+    // K/V loads start before the grid-dependency wait when the caller has stated
+    // that nothing still in flight writes the pool rows this call reads.
+    const int pre = my_tiles < C::ST ? my_tiles : C::ST;
+    if (p.prefetch_pool && lane == 0)
         for (int k = 0; k < pre; ++k) issue(k);
-    }
+    pdl_wait();
+    // Our predecessors are complete from here on, so a grid launched early after
+    // this trigger never overlaps a kernel older than this one.
+    pdl_launch_dependents();
+    if (!p.prefetch_pool && lane == 0)
+        for (int k = 0; k < pre; ++k) issue(k);
 
     // Q^T fragments (B operand): b0 = q[head g8][16ks + 2c4, +1], b1 = same + 8.
     // Heads >= G are zero columns.
@@ -205,6 +220,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             const uint32_t *w = reinterpret_cast<const uint32_t *>(qp + ks * 16 + 2 * c4);
             qf[ks][0] = real ? __ldg(w) : 0u;
             qf[ks][1] = real ? __ldg(w + 4) : 0u;
+        }
+    }
+
+    // Fused append: the first new row inside this slice is fetched now into the
+    // registers of the warp whose tile holds it (lanes [0, CH) carry K chunks,
+    // lanes [CH, 2CH) V chunks); any further new rows are read when met.
+    int pf_pos = -1;
+    uint4 pf = make_uint4(0u, 0u, 0u, 0u);
+    const bool row_lane = lane < 2 * CH;
+    const int rch = lane % CH;
+    const bool rv = lane >= CH;
+    auto new_row_chunk = [&](int pos) -> uint4 {
+        const T *src = static_cast<const T *>(rv ? p.v_new : p.k_new) +
+                       (static_cast<size_t>(pos + it.new_row_base) * p.num_kv_heads + it.kv_head) * D + rch * 8;
+        return __ldg(reinterpret_cast<const uint4 *>(src));
+    };
+    if (fused) {
+        const int nb = max(it.new_begin, it.tok_begin);
+        if (nb < it.tok_end && ((nb - it.tok_begin) / C::TW) % C::NW == warp) {
+            pf_pos = nb;
+            if (row_lane) pf = new_row_chunk(nb);
         }
     }
 
@@ -222,6 +258,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     bool ok = true;
     for (int k = 0; k < my_tiles; ++k) {
         const int s = k % C::ST;
+        // every lane observes the phase (TMA data visibility); the outcome is made warp-uniform
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, (k / C::ST) & 1))) {
             if (lane == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
             ok = false;
@@ -231,8 +268,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         const int tile = warp + k * C::NW;
         const int tb = it.tok_begin + tile * C::TW;
         const int nvalid = min(C::TW, it.tok_end - tb);
-        const uint32_t kb = smem_addr(pipe + (warp * C::ST + s) * C::STAGE_BYTES);
+        uint8_t *kp = pipe + (warp * C::ST + s) * C::STAGE_BYTES;
+        const uint32_t kb = smem_addr(kp);
         const uint32_t vb = kb + C::TILE_BYTES;
+
+        // ---- fused append: rows of this call's new tokens replace what the pool held
+        bool patched = false;
+        if (fused) {
+            const int nb = max(it.new_begin, tb);
+            if (nb < tb + nvalid) {  // warp-uniform
+                for (int pos = nb; pos < tb + nvalid; ++pos) {
+                    const uint4 val = (pos == pf_pos) ? pf : (row_lane ? new_row_chunk(pos) : pf);
+                    if (row_lane)
+                        *reinterpret_cast<uint4 *>(kp + (rv ? C::TILE_BYTES : 0) + tile_off<D>(pos - tb, rch)) = val;
+                }
+                patched = true;
+                __syncwarp();
+            }
+        }
 
         // ---- S^T = K . Q^T for the tile's m-tiles (rows = tokens)
         float sc[C::MT][4];
@@ -334,6 +387,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
                 M::mma(o[dt], a, pb_lo[mt][0], pb_lo[mt][1]);
             }
         }
+        if (patched) fence_proxy_async_smem();  // our stores precede the next TMA write of the stage
         __syncwarp();
         if (lane == 0 && k + C::ST < my_tiles) issue(k + C::ST);
     }
@@ -343,19 +397,40 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         for (int k = waited; k < issued; ++k) mbar_wait_bounded(bar0 + 8 * (k % C::ST), (k / C::ST) & 1);
     }
 
-    pdl_launch_dependents();
+    // ---- fused append: the item owning a query row stores that row's new K/V into the pool
+    if (fused && it.write_pos >= 0) {
+        const int pos = it.write_pos;
+        // the warp that prefetched this row stores it; otherwise warp 0 reads it again
+        const int nb = max(it.new_begin, it.tok_begin);
+        const bool held = nb < it.tok_end && nb == pos;
+        const int writer = held ? ((nb - it.tok_begin) / C::TW) % C::NW : 0;
+        if (warp == writer && row_lane) {
+            const int64_t page = p.kv_indices[it.page_base + pos / p.page_size];
+            if (page < 0 || page >= p.num_pages) {
+                if (rch == 0) atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
+            } else {
+                const uint4 val = held ? pf : new_row_chunk(pos);
+                T *dst = static_cast<T *>(rv ? p.v_pool : p.k_pool) +
+                         ((page * p.page_size + pos % p.page_size) * p.num_kv_heads + it.kv_head) * D + rch * 8;
+                *reinterpret_cast<uint4 *>(dst) = val;
+            }
+        }
+    }
 
-    // ---- combine the warps: per head column, (m, l, O)
+    // ---- combine the warps.  Per head column: M = max_w m_w, L = sum_w l_w 2^(m_w - M);
+    // each warp scales its O by 2^(m_w - M) / L, and the scaled partials are summed.
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
     }
-    __syncthreads();
+    constexpr int OS = D + 4;                     // padded row stride (floats) of the O buffer
+    __syncthreads();                              // pipeline stages are free from here on
     float *cm = reinterpret_cast<float *>(smem);  // [NW][8]
     float *cl = cm + C::NW * 8;                   // [NW][8]
-    float *co = cl + C::NW * 8;                   // [NW][8][D]
+    float *cf = cl + C::NW * 8;                   // [8] merged lse (log2) per head
+    float *co = cf + 8;                           // [NW][8][OS]
     if (g8 == 0) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -363,50 +438,71 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
             cl[warp * 8 + 2 * c4 + h] = l_run[h];
         }
     }
+    __syncthreads();
+    float f[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int hh = 2 * c4 + h;
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NW; ++w) Mx = fmaxf(Mx, cm[w * 8 + hh]);
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::NW; ++w) {
+            const float mw = cm[w * 8 + hh];
+            if (mw != -INFINITY) L += cl[w * 8 + hh] * exp2f(mw - Mx);
+        }
+        // L == 0 only when no key was admissible; a NaN (poisoned row) propagates.
+        f[h] = (m_run[h] == -INFINITY || L == 0.f) ? 0.f : exp2f(m_run[h] - Mx) / L;
+        if (warp == 0 && g8 == 0) cf[hh] = (L == 0.f) ? -INFINITY : Mx + log2f(L);
+    }
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt) {
-        float *ow = co + warp * 8 * D;
-        ow[(2 * c4) * D + dt * 16 + g8] = o[dt][0];
-        ow[(2 * c4 + 1) * D + dt * 16 + g8] = o[dt][1];
-        ow[(2 * c4) * D + dt * 16 + g8 + 8] = o[dt][2];
-        ow[(2 * c4 + 1) * D + dt * 16 + g8 + 8] = o[dt][3];
+        float *ow = co + (warp * 8 + 2 * c4) * OS + dt * 16 + g8;
+        ow[0] = o[dt][0] * f[0];
+        ow[OS] = o[dt][1] * f[1];
+        ow[8] = o[dt][2] * f[0];
+        ow[OS + 8] = o[dt][3] * f[1];
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < G * D; idx += C::NW * 32) {
-        const int h = idx / D;
-        const int c = idx - h * D;
-        float Mx = -INFINITY;
+    // Sum over warps; each thread produces 8 consecutive channels of one head.
+    for (int idx = threadIdx.x; idx < G * CH; idx += C::NW * 32) {
+        const int h = idx / CH;
+        const int c8 = (idx - h * CH) * 8;
+        float acc[8];
 #pragma unroll
-        for (int w = 0; w < C::NW; ++w) Mx = fmaxf(Mx, cm[w * 8 + h]);
-        float L = 0.f, O = 0.f;
-        if (Mx != -INFINITY) {
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll
-            for (int w = 0; w < C::NW; ++w) {
-                const float mw = cm[w * 8 + h];
-                if (mw != -INFINITY) {
-                    const float wt = exp2f(mw - Mx);
-                    L += cl[w * 8 + h] * wt;
-                    O += co[(w * 8 + h) * D + c] * wt;
-                }
-            }
+        for (int w = 0; w < C::NW; ++w) {
+            const float4 a = *reinterpret_cast<const float4 *>(co + (w * 8 + h) * OS + c8);
+            const float4 b = *reinterpret_cast<const float4 *>(co + (w * 8 + h) * OS + c8 + 4);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
         }
-        // L == 0 only for a slice with no admissible key; NaN (a poisoned row) propagates.
-        const float ov = L == 0.f ? 0.f : O / L;
-        const float lse2 = L == 0.f ? -INFINITY : Mx + log2f(L);
         const int head = it.kv_head * G + h;
         if (it.out_slot < 0) {
-            const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c;
-            if (p.out_dtype == PGQA_FP32)
-                static_cast<float *>(p.out)[oi] = ov;
-            else
-                static_cast<T *>(p.out)[oi] = narrow<T>(ov);
-            if (c == 0 && p.lse != nullptr)
-                p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = lse2 * 0.6931471805599453f;
+            const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c8;
+            if (p.out_dtype == PGQA_FP32) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + oi);
+                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            } else {
+                uint4 v;
+                v.x = M::pack(acc[0], acc[1]);
+                v.y = M::pack(acc[2], acc[3]);
+                v.z = M::pack(acc[4], acc[5]);
+                v.w = M::pack(acc[6], acc[7]);
+                *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + oi) = v;
+            }
+            if (c8 == 0 && p.lse != nullptr)
+                p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = cf[h] * 0.6931471805599453f;
         } else {
             const size_t slot = static_cast<size_t>(it.out_slot) * G + h;
-            p.partial_o[slot * D + c] = ov;
-            if (c == 0) p.partial_lse[slot] = lse2;
+            float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D + c8);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (c8 == 0) p.partial_lse[slot] = cf[h];
         }
     }
 }

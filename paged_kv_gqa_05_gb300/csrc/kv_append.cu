@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4 *__restrict__ k_po
                                                         const int64_t *__restrict__ slots,
                                                         int64_t num_tokens, int64_t num_slots,
                                                         int row_vecs, unsigned int *flags) {
+    pdl_launch_dependents();  // the next grid waits for our completion before reading the pool
     pdl_wait();
     const int64_t n = num_tokens * row_vecs;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -33,7 +34,6 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4 *__restrict__ k_po
         k_pool[s * row_vecs + vec] = __ldg(k + t * row_vecs + vec);
         v_pool[s * row_vecs + vec] = __ldg(v + t * row_vecs + vec);
     }
-    pdl_launch_dependents();
 }
 
 }  // namespace

@@ -7,9 +7,10 @@
 //     lse = log2 sum_s 2^lse_s,   o = sum_s 2^(lse_s - lse) o_s,
 // with empty slices (lse_s = -inf) carrying no weight.
 //
-// Grid: (merge task, head within the group, 32-channel chunk).  A block of 256
-// threads = 8 float4 columns x 32 slice groups, so a long list of slices is
-// read with many independent coalesced loads in flight.
+// Two launch shapes.  Up to 32 slices per row: one warp per (task, head), the
+// slice weights one per lane.  Longer lists: a block of 256 threads per (task,
+// head, 32-channel chunk) = 8 float4 columns x 32 slice groups, so a long list
+// is read with many independent coalesced loads in flight.
 #include <math.h>
 
 #include "common.cuh"
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     float *scratch = red + 32 * kChunk;      // [8]
     float *w = scratch + 8;                  // [num_splits]
 
+    pdl_launch_dependents();
     const MergeTask t = p.tasks[blockIdx.x];  // written by plan_update's copy only
     const int h = blockIdx.y;
     const int c0 = blockIdx.z * kChunk;
@@ -97,7 +99,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
     reinterpret_cast<float4 *>(red)[sg * 8 + c4] = acc;
     __syncthreads();
-    pdl_launch_dependents();
     if (threadIdx.x < kChunk) {
         float tot = 0.f;
 #pragma unroll 8
@@ -111,9 +112,77 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
 }
 
+// Short slice lists (<= 32 per row): one warp per (task, head).  Lane s holds the
+// weight of slice s; each lane owns D/32 consecutive channels of every slice.
+template <typename OutT, int D>
+__global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, int units) {
+    pdl_launch_dependents();
+    constexpr int V = D / 32;  // channels per lane: 2 (D = 64) or 4 (D = 128)
+    const int lane = threadIdx.x & 31;
+    const int u = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (u >= units) return;
+    const int G = p.group;
+    const MergeTask t = p.tasks[u / G];  // written by plan_update's copy only
+    const int h = u - (u / G) * G;
+    const int ns = t.num_splits;
+
+    pdl_wait();
+
+    const float l = lane < ns ? p.partial_lse[static_cast<size_t>(t.slot_base + lane) * G + h] : -INFINITY;
+    float mx = l;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    const float w = (l == -INFINITY) ? 0.f : exp2f(l - mx);  // NaN lse stays NaN
+    float sum = w;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+
+    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + lane * V;
+    const size_t stride = static_cast<size_t>(G) * D;
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < ns; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+        if (V == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
+            acc[0] += ws * v.x;
+            acc[1 % V] += ws * v.y;
+            acc[2 % V] += ws * v.z;
+            acc[3 % V] += ws * v.w;
+        } else {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(base + s * stride));
+            acc[0] += ws * v.x;
+            acc[1 % V] += ws * v.y;
+        }
+    }
+    const int head = t.kv_head * G + h;
+    const size_t oi = (static_cast<size_t>(t.q_row) * p.num_qo_heads + head) * D + lane * V;
+#pragma unroll
+    for (int j = 0; j < V; ++j) put<OutT>(p.out, oi + j, sum == 0.f ? 0.f : acc[j] / sum);
+    if (lane == 0 && p.lse != nullptr)
+        p.lse[static_cast<size_t>(t.q_row) * p.num_qo_heads + head] =
+            sum == 0.f ? -INFINITY : (mx + log2f(sum)) * 0.6931471805599453f;
+}
+
 template <typename OutT>
 cudaError_t launch_merge_t(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
                            cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    if (max_splits <= 32) {
+        const int units = num_tasks * p.group;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((units + 3) / 4);
+        cfg.blockDim = dim3(128);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 64>, p, units)
+                                : cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 128>, p, units);
+    }
     const size_t smem = (32 * kChunk + 8 + static_cast<size_t>(max_splits)) * sizeof(float);
     auto kern = merge_kernel<OutT>;
     if (smem > 48 * 1024) {
@@ -126,9 +195,6 @@ cudaError_t launch_merge_t(const MergeParams &p, int num_tasks, int max_splits, 
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
