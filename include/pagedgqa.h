@@ -123,6 +123,8 @@ typedef struct pgqa_plan_config {
     int ctas_per_sm;      /* occupancy target of the split heuristic; 0 = library default */
     int decode_kernel;    /* PGQA_DECODE_AUTO (tensor cores), PGQA_DECODE_TENSOR_CORE or
                              PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
+    int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
+                             per plan_update (3 when a whole slice fits in flight, else 2) */
 } pgqa_plan_config;
 
 #define PGQA_DECODE_AUTO 0

@@ -15,19 +15,19 @@
 #include "common.cuh"
 
 namespace pgqa {
-using DecodeLauncher = cudaError_t (*)(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &,
-                                        int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+using DecodeLauncher = cudaError_t (*)(int, int, int, const CUtensorMap &, const CUtensorMap &,
+                                        const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
 
-cudaError_t launch_decode(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
                           cudaStream_t stream) {
     DecodeLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_decode_bf16_d64 : launch_decode_bf16_d128)
                                           : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
-    return f(kind, group, tm_k, tm_v, p, num_items, pdl, stream);
+    return f(kind, stages, group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa
 
@@ -144,6 +144,7 @@ struct pgqa_plan {
     int box_rows = 0;
     int ctas_per_sm = 0;
     int kernel = PGQA_DECODE_TENSOR_CORE;
+    int stages = 2;     // per-warp pipeline depth of the tensor-core kernel (chosen per plan_update)
     int max_items = 0;  // capacity of the work list and of the partial slots
     int max_tasks = 0;
 
@@ -285,6 +286,8 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
     if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
         return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
+    if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
+        return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 2 or 3)", c.pipeline_stages);
 
     pgqa_plan *p = new (std::nothrow) pgqa_plan();
     if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
@@ -294,6 +297,7 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->box_rows = std::min(c.page_size, p->tile);
     p->ctas_per_sm = c.ctas_per_sm > 0 ? c.ctas_per_sm : 2;
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
+    p->stages = c.pipeline_stages == 3 ? 3 : 2;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e != cudaSuccess) {
@@ -492,6 +496,14 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     plan->staged_used[buf] = true;
     plan->cur ^= 1;
 
+    // Pipeline depth: three stages when every warp's tiles of the longest slice can be
+    // requested at once (the whole slice in flight from the start), two otherwise so
+    // that three CTAs fit on an SM and overlap each other's set-up and epilogue.
+    if (c.pipeline_stages == 0) {
+        int64_t longest_item = 0;
+        for (const WorkItem &w : items) longest_item = std::max<int64_t>(longest_item, w.tok_end - w.tok_begin);
+        plan->stages = longest_item <= 3LL * kDecodeWarps * tile ? 3 : 2;
+    }
     plan->n_items = static_cast<int>(items.size());
     plan->n_tasks = static_cast<int>(tasks.size());
     plan->split_tokens = static_cast<int>(ls);
@@ -566,7 +578,8 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.num_kv_heads = c.num_kv_heads;
     p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_decode(plan->kernel, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items, true, st);
+    e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,
+                      true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (plan->n_tasks > 0) {
         MergeParams mp{};

@@ -42,7 +42,7 @@ struct alignas(16) MergeTask {
 static_assert(sizeof(MergeTask) == 16, "MergeTask is 16 bytes");
 
 // Warp tile (tokens one warp owns per pipeline stage) of the decode kernel.
-constexpr int decode_warp_tile(int head_dim) { return head_dim == 64 ? 32 : 16; }
+__host__ __device__ constexpr int decode_warp_tile(int head_dim) { return head_dim == 64 ? 32 : 16; }
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 3;
 
@@ -85,7 +85,7 @@ struct MergeParams {
 };
 
 // Launchers (defined in the kernel translation units).
-cudaError_t launch_decode(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items,
                           bool pdl, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
@@ -216,6 +216,32 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Hardware approximations (PTX ex2/lg2/rcp .approx): a few ulp, ample for the
+// softmax weights and the log-sum-exp.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Named barrier 1 over `count` threads: producers arrive, the consumer waits.
+__device__ __forceinline__ void named_bar_arrive(int count) {
+    asm volatile("bar.arrive 1, %0;" ::"r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int count) {
+    asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
 }
 
 // 16-byte shared-memory load through a plain C++ access, so the compiler orders

@@ -87,13 +87,13 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
 template <typename T>
 __device__ __forceinline__ float2 unpack2(uint32_t v) { return widen2<T>(v); }
 
-template <int D>
+template <int D, int STAGES>
 struct TcCfg {
     static constexpr int TW = decode_warp_tile(D);      // tokens per warp tile (32 for d64, 16 for d128)
     static constexpr int MT = TW / 16;                   // token m-tiles per warp tile
     static constexpr int HALVES = D / 64;                // 128-byte (64-channel) column blocks per row
     static constexpr int NW = kDecodeWarps;
-    static constexpr int ST = kDecodeStages;
+    static constexpr int ST = STAGES;
     static constexpr int HALF_BYTES = TW * 128;          // one 64-channel block of a tile
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K tile, then V tile
@@ -101,9 +101,10 @@ struct TcCfg {
     static constexpr int BAR_BYTES = NW * ST * 8;
     static constexpr int DT = D / 16;                    // d m-tiles of the PV product
     static constexpr int KS = D / 16;                    // k-steps of the QK product
-    static constexpr int COMBINE_BYTES = (NW * 8 * 2 + 8 + NW * 8 * (D + 4)) * 4;
+    static constexpr int OS = D + 4;                     // padded row stride (floats) of a warp's O
+    static constexpr int WARP_COMBINE_BYTES = (16 + 8 * OS) * 4;
     static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4;
-    static_assert(COMBINE_BYTES <= PIPE_BYTES, "combine buffer reuses the stages");
+    static_assert(WARP_COMBINE_BYTES <= ST * STAGE_BYTES, "a warp's combine state fits its own stages");
     static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
 };
 
@@ -111,14 +112,14 @@ struct TcCfg {
 // K or V tile, as the 128B-swizzled TMA boxes lay it out.
 template <int D>
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
-    return (c >> 3) * TcCfg<D>::HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+    return (c >> 3) * (decode_warp_tile(D) * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, typename T>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 2)
+template <int D, int STAGES, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p, int G) {
-    using C = TcCfg<D>;
+    using C = TcCfg<D, STAGES>;
     using M = MmaType<T>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const float mn = fmaxf(m_run[h], mx[h]);
-            alpha[h] = (mn == m_run[h]) ? 1.f : exp2f(m_run[h] - mn);
+            alpha[h] = (mn == m_run[h]) ? 1.f : ex2_approx(m_run[h] - mn);
             m_run[h] = mn;
             l_run[h] *= alpha[h];
         }
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float x = sc[mt][j];
-                pr[j] = (x == -INFINITY) ? 0.f : exp2f(x - m_run[j & 1]);
+                pr[j] = (x == -INFINITY) ? 0.f : ex2_approx(x - m_run[j & 1]);
                 l_run[j & 1] += pr[j];
             }
             // rows g8 (j = 0, 1) and g8 + 8 (j = 2, 3); columns 2c4, 2c4 + 1
@@ -405,7 +406,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         const bool held = nb < it.tok_end && nb == pos;
         const int writer = held ? ((nb - it.tok_begin) / C::TW) % C::NW : 0;
         if (warp == writer && row_lane) {
-            const int64_t page = p.kv_indices[it.page_base + pos / p.page_size];
+            const int64_t page = (pos >= it.tok_begin && pos < it.tok_end)
+                                     ? pages(pos, p.page_size)
+                                     : p.kv_indices[it.page_base + pos / p.page_size];
             if (page < 0 || page >= p.num_pages) {
                 if (rch == 0) atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
             } else {
@@ -417,101 +420,125 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
         }
     }
 
-    // ---- combine the warps.  Per head column: M = max_w m_w, L = sum_w l_w 2^(m_w - M);
-    // each warp scales its O by 2^(m_w - M) / L, and the scaled partials are summed.
+    // ---- combine the warps.  Per head column: M = max_w m_w, L = sum_w l_w 2^(m_w - M),
+    // O = sum_w 2^(m_w - M) O_w / L.  Each warp leaves (m, l, O) in its own stage area
+    // (its TMA copies have all landed) and warps 1.. exit; warp 0 combines.
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
     }
-    constexpr int OS = D + 4;                     // padded row stride (floats) of the O buffer
-    __syncthreads();                              // pipeline stages are free from here on
-    float *cm = reinterpret_cast<float *>(smem);  // [NW][8]
-    float *cl = cm + C::NW * 8;                   // [NW][8]
-    float *cf = cl + C::NW * 8;                   // [8] merged lse (log2) per head
-    float *co = cf + 8;                           // [NW][8][OS]
-    if (g8 == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            cm[warp * 8 + 2 * c4 + h] = m_run[h];
-            cl[warp * 8 + 2 * c4 + h] = l_run[h];
+    constexpr int OS = C::OS;
+    auto state = [&](int w) { return reinterpret_cast<float *>(pipe + w * C::ST * C::STAGE_BYTES); };
+    if (warp != 0) {
+        float *st = state(warp);  // [8] m, [8] l, [8][OS] O
+        if (g8 == 0) {
+            st[2 * c4] = m_run[0];
+            st[2 * c4 + 1] = m_run[1];
+            st[8 + 2 * c4] = l_run[0];
+            st[8 + 2 * c4 + 1] = l_run[1];
         }
+#pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt) {
+            float *ow = st + 16 + (2 * c4) * OS + dt * 16 + g8;
+            ow[0] = o[dt][0];
+            ow[OS] = o[dt][1];
+            ow[8] = o[dt][2];
+            ow[OS + 8] = o[dt][3];
+        }
+        named_bar_arrive(C::NW * 32);
+        return;
     }
-    __syncthreads();
-    float f[2];
+    named_bar_sync(C::NW * 32);
+
+    float f[C::NW][2], lse2[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int hh = 2 * c4 + h;
-        float Mx = -INFINITY;
+        float Mx = m_run[h];
 #pragma unroll
-        for (int w = 0; w < C::NW; ++w) Mx = fmaxf(Mx, cm[w * 8 + hh]);
-        float L = 0.f;
+        for (int w = 1; w < C::NW; ++w) Mx = fmaxf(Mx, state(w)[hh]);
+        float L = (m_run[h] == -INFINITY) ? 0.f : l_run[h] * ex2_approx(m_run[h] - Mx);
 #pragma unroll
-        for (int w = 0; w < C::NW; ++w) {
-            const float mw = cm[w * 8 + hh];
-            if (mw != -INFINITY) L += cl[w * 8 + hh] * exp2f(mw - Mx);
+        for (int w = 1; w < C::NW; ++w) {
+            const float mw = state(w)[hh];
+            if (mw != -INFINITY) L += state(w)[8 + hh] * ex2_approx(mw - Mx);
         }
         // L == 0 only when no key was admissible; a NaN (poisoned row) propagates.
-        f[h] = (m_run[h] == -INFINITY || L == 0.f) ? 0.f : exp2f(m_run[h] - Mx) / L;
-        if (warp == 0 && g8 == 0) cf[hh] = (L == 0.f) ? -INFINITY : Mx + log2f(L);
+        const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
+        f[0][h] = (m_run[h] == -INFINITY) ? 0.f : ex2_approx(m_run[h] - Mx) * inv;
+#pragma unroll
+        for (int w = 1; w < C::NW; ++w) {
+            const float mw = state(w)[hh];
+            f[w][h] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - Mx) * inv;
+        }
+        lse2[h] = (L == 0.f) ? -INFINITY : Mx + lg2_approx(L);
     }
+    float *fin = state(0) + 16;  // [8][OS] final O of this slice, staged for vector stores
 #pragma unroll
     for (int dt = 0; dt < C::DT; ++dt) {
-        float *ow = co + (warp * 8 + 2 * c4) * OS + dt * 16 + g8;
-        ow[0] = o[dt][0] * f[0];
-        ow[OS] = o[dt][1] * f[1];
-        ow[8] = o[dt][2] * f[0];
-        ow[OS + 8] = o[dt][3] * f[1];
-    }
-    __syncthreads();
-
-    // Sum over warps; each thread produces 8 consecutive channels of one head.
-    for (int idx = threadIdx.x; idx < G * CH; idx += C::NW * 32) {
-        const int h = idx / CH;
-        const int c8 = (idx - h * CH) * 8;
-        float acc[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int j = 0; j < 4; ++j) {
+            const int h = j & 1;
+            const int off = (2 * c4 + h) * OS + dt * 16 + g8 + (j >> 1) * 8;
+            float acc = o[dt][j] * f[0][h];
 #pragma unroll
-        for (int w = 0; w < C::NW; ++w) {
-            const float4 a = *reinterpret_cast<const float4 *>(co + (w * 8 + h) * OS + c8);
-            const float4 b = *reinterpret_cast<const float4 *>(co + (w * 8 + h) * OS + c8 + 4);
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            for (int w = 1; w < C::NW; ++w) acc += state(w)[16 + off] * f[w][h];
+            fin[off] = acc;
         }
+    }
+    __syncwarp();
+
+    constexpr int CH8 = D / 8;
+    for (int idx = lane; idx < G * CH8; idx += 32) {
+        const int h = idx / CH8;
+        const int c8 = (idx - h * CH8) * 8;
+        const float4 a = *reinterpret_cast<const float4 *>(fin + h * OS + c8);
+        const float4 b = *reinterpret_cast<const float4 *>(fin + h * OS + c8 + 4);
         const int head = it.kv_head * G + h;
         if (it.out_slot < 0) {
             const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c8;
             if (p.out_dtype == PGQA_FP32) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + oi);
-                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                dst[0] = a;
+                dst[1] = b;
             } else {
                 uint4 v;
-                v.x = M::pack(acc[0], acc[1]);
-                v.y = M::pack(acc[2], acc[3]);
-                v.z = M::pack(acc[4], acc[5]);
-                v.w = M::pack(acc[6], acc[7]);
+                v.x = M::pack(a.x, a.y);
+                v.y = M::pack(a.z, a.w);
+                v.z = M::pack(b.x, b.y);
+                v.w = M::pack(b.z, b.w);
                 *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + oi) = v;
             }
-            if (c8 == 0 && p.lse != nullptr)
-                p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = cf[h] * 0.6931471805599453f;
         } else {
-            const size_t slot = static_cast<size_t>(it.out_slot) * G + h;
-            float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D + c8);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            if (c8 == 0) p.partial_lse[slot] = cf[h];
+            float4 *dst = reinterpret_cast<float4 *>(p.partial_o + (static_cast<size_t>(it.out_slot) * G + h) * D + c8);
+            dst[0] = a;
+            dst[1] = b;
+        }
+    }
+    if (g8 == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int hh = 2 * c4 + h;
+            if (hh < G) {
+                const int head = it.kv_head * G + hh;
+                if (it.out_slot < 0) {
+                    if (p.lse != nullptr)
+                        p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = lse2[h] * 0.6931471805599453f;
+                } else {
+                    p.partial_lse[static_cast<size_t>(it.out_slot) * G + hh] = lse2[h];
+                }
+            }
         }
     }
 }
 
-template <int D, typename T>
-cudaError_t launch_decode_tc(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
-                             int num_items, bool pdl, cudaStream_t stream) {
-    using C = TcCfg<D>;
-    auto kern = decode_tc_kernel<D, T>;
+template <int D, int STAGES, typename T>
+cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
+                                int num_items, bool pdl, cudaStream_t stream) {
+    using C = TcCfg<D, STAGES>;
+    auto kern = decode_tc_kernel<D, STAGES, T>;
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -533,6 +560,13 @@ cudaError_t launch_decode_tc(int group, const CUtensorMap &tm_k, const CUtensorM
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p, group);
+}
+
+template <int D, typename T>
+cudaError_t launch_decode_tc(int stages, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                             const DecodeParams &p, int num_items, bool pdl, cudaStream_t stream) {
+    return stages == 3 ? launch_decode_tc_st<D, 3, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                       : launch_decode_tc_st<D, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 }  // namespace pgqa
