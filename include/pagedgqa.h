@@ -231,6 +231,40 @@ PGQA_API pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const v
                                      void *k_pool, void *v_pool, void *out, pgqa_dtype out_dtype, float *lse,
                                      float sm_scale, int flags, pgqa_stream_t stream);
 
+/*
+ * pgqa_decode_static_scratch -- split-KV decode that allocates nothing.
+ *
+ * None of the pages has a counterpart to this call; it serves callers that
+ * cannot allocate device memory: code running while a CUDA graph is being
+ * captured (allocation would break the capture), runtimes that hand all device
+ * memory to their own allocator, and embedded hosts without an allocator.  It
+ * needs no plan: the slices are cut on the device from the device-side page
+ * table, and the work list, merge list and split partials live in one 8 MiB
+ * array inside the library (a static device array, held by every GPU that loads
+ * the library until the process exits).  No cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ *
+ *   q            [batch, num_qo_heads, head_dim]: one decode row per request
+ *   k_pool/v_pool, kv_indices  as for pgqa_plan_update / pgqa_run
+ *   kv_indptr    [batch+1] int32, DEVICE
+ *   last_page_len [batch] int32, DEVICE (values outside [1, page_size] for a
+ *                request with pages are clamped and raise PGQA_FLAG_PAGE_INDEX)
+ *   splits       slices per (request, kv head), 1..256 (1 = no merge)
+ *   out, out_dtype, lse, sm_scale  as for pgqa_run
+ * batch * num_kv_heads * splits must fit the array (about 8 MiB of work items
+ * and fp32 partials); otherwise PGQA_ERR_CAPACITY and nothing is launched.
+ * The first call on a device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.  All
+ * calls share the array: calls whose kernels may overlap on the GPU (different
+ * streams without ordering) race.  Nothing in the array needs to start zeroed.
+ */
+PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const void *k_pool, const void *v_pool,
+                                                const int32_t *kv_indptr, const int32_t *kv_indices,
+                                                const int32_t *last_page_len, int batch, int64_t num_pages,
+                                                int page_size, int num_qo_heads, int num_kv_heads, int head_dim,
+                                                pgqa_dtype dtype, int splits, void *out, pgqa_dtype out_dtype,
+                                                float *lse, float sm_scale, pgqa_stream_t stream);
+
 /* Frees the plan's buffers (synchronising with its last enqueued copy).  NULL is a no-op. */
 PGQA_API pgqa_status pgqa_plan_destroy(pgqa_plan *plan);
 

@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "PGQA_OK", 1: "PGQA_ERR_INVALID_ARG", 2: "PGQA_ERR_UNSUPPORTE
 # Every entry point include/pagedgqa.h declares.
 EXPORTS = ("pgqa_abi_version", "pgqa_status_string", "pgqa_last_error", "pgqa_read_device_flags",
            "pgqa_kv_append", "pgqa_plan_create", "pgqa_plan_update", "pgqa_run",
-           "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run")
+           "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run", "pgqa_decode_static_scratch")
 
 
 class PagedGQAError(RuntimeError):
@@ -89,6 +89,11 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_append_run.restype = ctypes.c_int
     lib.pgqa_append_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_float,
                                     ctypes.c_int, _vp]
+    lib.pgqa_decode_static_scratch.restype = ctypes.c_int
+    lib.pgqa_decode_static_scratch.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                                               ctypes.c_float, _vp]
     lib.pgqa_plan_destroy.restype = ctypes.c_int
     lib.pgqa_plan_destroy.argtypes = [_vp]
     lib.pgqa_plan_get_info.restype = ctypes.c_int
@@ -224,6 +229,28 @@ def append_run(plan: int, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Ten
                                   _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dev(out, "out"),
                                   TORCH_TO_CODE[out.dtype], None if lse is None else _dev(lse, "lse"),
                                   float(sm_scale), POOL_STABLE if pool_stable else 0, _stream(stream)))
+    return out
+
+
+def decode_static_scratch(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                          kv_indptr: torch.Tensor, kv_indices: torch.Tensor, last_page_len: torch.Tensor,
+                          splits: int, out: Optional[torch.Tensor] = None,
+                          out_dtype: Optional[torch.dtype] = None, lse: Optional[torch.Tensor] = None,
+                          sm_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """pgqa_decode_static_scratch: decode without any device allocation inside the
+    library (page table on the device).  `out` should be preallocated by callers
+    that cannot allocate."""
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    for t, name in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (last_page_len, "last_page_len")):
+        if t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    P, ps, Hkv, D = k_pool.shape
+    _check(load().pgqa_decode_static_scratch(
+        _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dev(kv_indptr, "kv_indptr"),
+        _dev(kv_indices, "kv_indices") if kv_indices.numel() else None, _dev(last_page_len, "last_page_len"),
+        q.shape[0], P, ps, q.shape[1], Hkv, D, TORCH_TO_CODE[q.dtype], int(splits), _dev(out, "out"),
+        TORCH_TO_CODE[out.dtype], None if lse is None else _dev(lse, "lse"), float(sm_scale), _stream(stream)))
     return out
 
 

@@ -209,6 +209,17 @@ static void plan_free(pgqa_plan *p) {
     delete p;
 }
 
+// Helpers shared with the other entry-point translation units.
+namespace pgqa {
+pgqa_status report(pgqa_status s, const char *msg) { return fail(s, "%s", msg); }
+pgqa_status report_cuda(cudaError_t e, const char *what) { return cuda_fail(e, what); }
+pgqa_status current_device_flags(unsigned int **out) { return device_flags(out); }
+pgqa_status encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages, int page_size, int num_kv_heads,
+                            int head_dim, pgqa_dtype dt, int box_rows, bool swizzle128) {
+    return make_pool_map(map, pool, num_pages, page_size, num_kv_heads, head_dim, dt, box_rows, swizzle128);
+}
+}  // namespace pgqa
+
 extern "C" {
 
 int pgqa_abi_version(void) { return PGQA_ABI_VERSION; }

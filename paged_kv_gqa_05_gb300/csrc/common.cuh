@@ -94,6 +94,13 @@ cudaError_t launch_kv_append(void *k_pool, void *v_pool, const void *k, const vo
                              const int64_t *slot_mapping, int64_t num_tokens, int64_t num_slots,
                              int row_bytes, unsigned int *flags, bool pdl, cudaStream_t stream);
 
+// Host helpers defined in api.cu.
+pgqa_status report(pgqa_status s, const char *msg);
+pgqa_status report_cuda(cudaError_t e, const char *what);
+pgqa_status current_device_flags(unsigned int **out);
+pgqa_status encode_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages, int page_size, int num_kv_heads,
+                            int head_dim, pgqa_dtype dt, int box_rows, bool swizzle128);
+
 // ---------------------------------------------------------------------------
 // Device helpers (inline PTX)
 // ---------------------------------------------------------------------------
