@@ -82,6 +82,43 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
 # peaks and clocks
 # ---------------------------------------------------------------------------
 
+PROFILE_FILES = {"qwen05_decode": "decode_tc_qwen05_decode_128x301.md",
+                 "long_context_b4": "decode_tc_long_context_b4_32768.md"}
+KERNEL_SOURCES = ("paged_kv_gqa_05_gb300/csrc/decode_tc.cuh", "paged_kv_gqa_05_gb300/csrc/common.cuh")
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when there is
+    none for this workload or the kernel source changed after it was taken."""
+    name = PROFILE_FILES.get(workload)
+    if not name:
+        return None
+    fields = {}
+    try:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+    except OSError:
+        return None
+    if fields.get("kernel_sources_sha256_16") != kernel_sources_hash():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -327,8 +364,18 @@ def run_ours(args, rank, world, local):
     total_bytes = sum_over_ranks(b["per_step"] * args.steps, world, device)
     value = total_bytes / t_dev / 1e9
     peak, peak_src = hbm_peak()
-    per_launch_s = t_run / (run_reps * layers)
-    achieved = b["attention_per_layer"] / per_launch_s / 1e9
+    if per_layer_launches == 1 and not args.no_graph:
+        # the decode kernel is the only launch of a layer: its average duration is the
+        # timed step divided by the launches in it (append bytes are part of its work)
+        per_launch_s = t_dev / (args.steps * layers)
+        launch_bytes = b["attention_per_layer"] + b["append_per_layer"]
+        timing_note = "timed step / launches (one decode_tc launch per layer), events on the launch stream"
+    else:
+        per_launch_s = t_run / (run_reps * layers)
+        launch_bytes = b["attention_per_layer"]
+        timing_note = "run()-only CUDA graph over the layer pools, events on the launch stream"
+    achieved = launch_bytes / per_launch_s / 1e9
+    traffic = profiled_traffic(args.workload) if args.decode_kernel != "cuda_core" else None
     e2e_value = sum_over_ranks(b["per_step"] * args.steps, world, device) / t_e2e / 1e9
 
     result = {
@@ -357,13 +404,16 @@ def run_ours(args, rank, world, local):
                                           "num_sms")},
         },
         "us_per_layer": round(t_dev / args.steps / layers * 1e6, 3),
-        "us_per_run_call": round(per_launch_s * 1e6, 3),
+        "us_per_run_call": round(t_run / (run_reps * layers) * 1e6, 3),
+        "us_per_decode_launch": round(per_launch_s * 1e6, 3),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "bytes": b,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
-                     "kernel": "decode_partial_kernel (+ merge_kernel when rows are split)",
-                     "timing": "run()-only CUDA graph over the layer pools, events on the launch stream"},
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": launch_bytes,
+                     "kernel": ("decode_cuda_core" if args.decode_kernel == "cuda_core" else "decode_tc_kernel")
+                               + (" (+ merge_kernel)" if info["num_merge_tasks"] else ""),
+                     "timing": timing_note},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(L["inputs"].numel() * L["inputs"].element_size()),
                 "d2h_bytes_per_step": int(L["out"].numel() * L["out"].element_size())},

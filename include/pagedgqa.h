@@ -125,6 +125,7 @@ typedef struct pgqa_plan_config {
                              PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
     int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
                              per plan_update (3 when a whole slice fits in flight, else 2) */
+    int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
 } pgqa_plan_config;
 
 #define PGQA_DECODE_AUTO 0
@@ -277,6 +278,7 @@ typedef struct pgqa_plan_info {
     int total_q_rows;
     int num_sms;            /* SMs of the plan's device */
     int64_t kv_tokens;      /* sum of kv_len over requests */
+    int num_prefill_tiles;  /* CTAs of the prefill-segment kernel (requests with > 1 query row) */
 } pgqa_plan_info;
 
 PGQA_API pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info);

@@ -29,6 +29,20 @@ cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dt
                                           : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
     return f(kind, stages, group, tm_k, tm_v, p, num_items, pdl, stream);
 }
+using PrefillLauncher = cudaError_t (*)(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int,
+                                         bool, cudaStream_t);
+cudaError_t launch_prefill_bf16_d64(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_bf16_d128(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_fp16_d64(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_fp16_d128(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+
+cudaError_t launch_prefill(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+                           const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
+                           cudaStream_t stream) {
+    PrefillLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_prefill_bf16_d64 : launch_prefill_bf16_d128)
+                                           : (head_dim == 64 ? launch_prefill_fp16_d64 : launch_prefill_fp16_d128);
+    return f(group, tm_k, tm_v, p, num_items, pdl, stream);
+}
 }  // namespace pgqa
 
 using namespace pgqa;
@@ -132,6 +146,7 @@ static int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 struct MapCacheEntry {
     const void *ptr = nullptr;
     int64_t num_pages = 0;
+    int box_rows = 0;
     CUtensorMap map;
 };
 
@@ -147,8 +162,10 @@ struct pgqa_plan {
     int stages = 2;     // per-warp pipeline depth of the tensor-core kernel (chosen per plan_update)
     int max_items = 0;  // capacity of the work list and of the partial slots
     int max_tasks = 0;
+    int max_prefill = 0;     // capacity of the prefill-tile list
+    int max_slots = 0;       // capacity of the split partials (slots of G x head_dim floats)
 
-    void *d_meta = nullptr;  // [max_items] WorkItem then [max_tasks] MergeTask
+    void *d_meta = nullptr;  // [max_items] WorkItem, [max_tasks] MergeTask, [max_prefill] PrefillItem
     float *d_partial_o = nullptr;
     float *d_partial_lse = nullptr;
     void *h_meta[2] = {nullptr, nullptr};
@@ -159,6 +176,8 @@ struct pgqa_plan {
     bool valid = false;
     int n_items = 0, n_tasks = 0, split_tokens = 0, max_splits_used = 0, total_q_rows = 0;
     int max_task_splits = 0;
+    int n_prefill = 0;
+    bool causal = false;
     bool fusable = false;  // every request has at least as many keys as query rows
     int64_t kv_tokens = 0, num_pages = 0;
     const int32_t *kv_indices = nullptr;
@@ -171,25 +190,28 @@ struct pgqa_plan {
     MergeTask *tasks() {
         return reinterpret_cast<MergeTask *>(static_cast<char *>(d_meta) + sizeof(WorkItem) * max_items);
     }
+    size_t prefill_offset() const { return sizeof(WorkItem) * max_items + sizeof(MergeTask) * max_tasks; }
+    PrefillItem *prefill_items() { return reinterpret_cast<PrefillItem *>(static_cast<char *>(d_meta) + prefill_offset()); }
 };
 
-static pgqa_status pool_map(pgqa_plan *plan, const void *pool, const CUtensorMap **out) {
+static pgqa_status pool_map(pgqa_plan *plan, const void *pool, int box_rows, bool swizzle128,
+                            const CUtensorMap **out) {
     for (auto &e : plan->maps)
-        if (e.ptr == pool && e.num_pages == plan->num_pages) {
+        if (e.ptr == pool && e.num_pages == plan->num_pages && e.box_rows == box_rows) {
             *out = &e.map;
             return PGQA_OK;
         }
     MapCacheEntry &e = plan->maps[plan->map_next];
     plan->map_next = (plan->map_next + 1) % pgqa_plan::kMapCache;
     pgqa_status s = make_pool_map(&e.map, pool, plan->num_pages, plan->cfg.page_size, plan->cfg.num_kv_heads,
-                                  plan->cfg.head_dim, plan->cfg.dtype, plan->box_rows,
-                                  plan->kernel == PGQA_DECODE_TENSOR_CORE);
+                                  plan->cfg.head_dim, plan->cfg.dtype, box_rows, swizzle128);
     if (s != PGQA_OK) {
         e.ptr = nullptr;
         return s;
     }
     e.ptr = pool;
     e.num_pages = plan->num_pages;
+    e.box_rows = box_rows;
     *out = &e.map;
     return PGQA_OK;
 }
@@ -297,6 +319,8 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
     if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
         return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
+    if (c.prefill_splits < 0 || c.prefill_splits > 8)
+        return fail(PGQA_ERR_INVALID_ARG, "prefill_splits %d (0..8)", c.prefill_splits);
     if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
         return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 2 or 3)", c.pipeline_stages);
 
@@ -323,13 +347,17 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     }
     p->max_items = static_cast<int>(items);
     p->max_tasks = static_cast<int>(c.max_q_rows * c.num_kv_heads);
-    const size_t meta = sizeof(WorkItem) * p->max_items + sizeof(MergeTask) * p->max_tasks;
+    p->max_prefill = static_cast<int>((c.max_q_rows * group / 64 + c.max_batch + 1) * c.num_kv_heads * 8);
+    // partial slots: split decode slices, plus up to 8 key slices per prefill row and kv head
+    p->max_slots = p->max_items + static_cast<int>(c.max_q_rows * c.num_kv_heads * 8);
+    const size_t meta = sizeof(WorkItem) * p->max_items + sizeof(MergeTask) * p->max_tasks +
+                        sizeof(PrefillItem) * p->max_prefill;
     e = cudaMalloc(&p->d_meta, meta);
     if (e == cudaSuccess)
         e = cudaMalloc(reinterpret_cast<void **>(&p->d_partial_o),
-                       sizeof(float) * static_cast<size_t>(p->max_items) * group * c.head_dim);
+                       sizeof(float) * static_cast<size_t>(p->max_slots) * group * c.head_dim);
     if (e == cudaSuccess)
-        e = cudaMalloc(reinterpret_cast<void **>(&p->d_partial_lse), sizeof(float) * static_cast<size_t>(p->max_items) * group);
+        e = cudaMalloc(reinterpret_cast<void **>(&p->d_partial_lse), sizeof(float) * static_cast<size_t>(p->max_slots) * group);
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
         e = cudaMallocHost(&p->h_meta[i], meta);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->staged[i], cudaEventDisableTiming);
@@ -356,6 +384,7 @@ pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info) {
     info->total_q_rows = plan->total_q_rows;
     info->num_sms = plan->num_sms;
     info->kv_tokens = plan->kv_tokens;
+    info->num_prefill_tiles = plan->n_prefill;
     return PGQA_OK;
 }
 
@@ -409,6 +438,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     rowv.reserve(static_cast<size_t>(rows));
     int64_t work = 0, kv_tokens = 0;
     bool fusable = true;
+    std::vector<PrefillItem> prefill;
     for (int b = 0; b < batch; ++b) {
         const int64_t np = static_cast<int64_t>(kv_indptr[b + 1]) - kv_indptr[b];
         const int64_t n = np == 0 ? 0 : (np - 1) * c.page_size + last_page_len[b];
@@ -418,6 +448,21 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         // A fused append writes the request's last L key positions from the L new rows.
         if (L > n) fusable = false;
         const int64_t nb = L <= n ? n - L : INT32_MAX;
+        if (L > 1 && plan->kernel == PGQA_DECODE_TENSOR_CORE) {
+            // A chunk of rows: tensor-core prefill tiles of 64 (row, head) pairs per kv head
+            // (key slices are assigned below, once all tiles are known).
+            const int G = plan->group;
+            for (int kvh = 0; kvh < c.num_kv_heads; ++kvh)
+                for (int64_t m0 = 0; m0 < L * G; m0 += 64) {
+                    const int64_t i_last = std::min<int64_t>(L - 1, (m0 + 63) / G);
+                    int64_t kend = causal ? n - L + i_last + 1 : n;
+                    kend = std::max<int64_t>(0, std::min<int64_t>(n, kend));
+                    prefill.push_back({kv_indptr[b], 0, static_cast<int32_t>(kend), static_cast<int32_t>(r0),
+                                       static_cast<int32_t>(L), static_cast<int32_t>(n), kvh,
+                                       static_cast<int32_t>(m0), -1, 0, 1, 0});
+                }
+            continue;
+        }
         for (int64_t r = r0; r < r1; ++r) {
             int64_t a = n;
             if (causal) a = std::min<int64_t>(n, std::max<int64_t>(0, n - L + (r - r0) + 1));
@@ -429,23 +474,48 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     }
     work *= c.num_kv_heads;
 
-    // Slice length: enough slices to fill num_sms * ctas_per_sm CTAs, each a whole
-    // number of warp tiles and at least one tile per warp.
     const int tile = plan->tile;
     const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
     int64_t ls;
-    const int64_t pairs = static_cast<int64_t>(rowv.size()) * c.num_kv_heads;
     int64_t longest = 0;
     for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
     if (c.split_tokens > 0) {
         ls = round_up(c.split_tokens, tile);
-    } else if (pairs >= plan->num_sms) {
-        // Every SM already has a (row, kv head) of its own: a split would only add
-        // per-CTA set-up and a merge.
-        ls = std::max<int64_t>(min_split, round_up(std::max<int64_t>(1, longest), tile));
     } else {
-        const int64_t target = static_cast<int64_t>(plan->num_sms) * plan->ctas_per_sm;
-        ls = std::max<int64_t>(min_split, round_up(std::max<int64_t>(1, ceil_div(work, target)), tile));
+        // Pick the slice length (whole warp tiles, at least one tile per warp) that
+        // minimises a makespan estimate over num_sms * ctas_per_sm CTA slots, in bytes:
+        //   max(total / slots, longest slice) + per-CTA set-up x CTAs per slot
+        //   (+ the merge launch once any row is split).
+        // Uniform short rows stay whole; long rows are cut near the per-slot share.
+        const double slots = static_cast<double>(plan->num_sms) * plan->ctas_per_sm;
+        const double row_bytes = 4.0 * c.head_dim;  // K + V of one token of one kv head
+        const double cta_cost = 24.0 * 1024, merge_cost = 40.0 * 1024;
+        const double share = static_cast<double>(work) * row_bytes / slots;
+        const int64_t k_lo = min_split / tile;
+        const int64_t k_hi = std::max<int64_t>(k_lo, ceil_div(std::max<int64_t>(1, longest), tile));
+        double best = 0.0;
+        ls = k_hi * tile;
+        for (int64_t k = k_hi; k >= k_lo; --k) {
+            const int64_t len = k * tile;
+            int64_t n_items = 0, max_slice = 0;
+            bool split = false;
+            for (const Row &rw : rowv) {
+                int64_t ns = rw.n == 0 ? 1 : ceil_div(rw.n, len);
+                if (c.max_splits > 0) ns = std::min<int64_t>(ns, c.max_splits);
+                const int64_t sl = rw.n == 0 ? 0 : round_up(ceil_div(rw.n, ns), tile);
+                n_items += ns;
+                max_slice = std::max(max_slice, std::min<int64_t>(sl, rw.n));
+                split = split || ns > 1;
+            }
+            n_items *= c.num_kv_heads;
+            const double est = std::max(share, max_slice * row_bytes) + cta_cost * std::ceil(n_items / slots) +
+                               (split ? merge_cost : 0.0);
+            if (k == k_hi || est < best) {
+                best = est;
+                ls = len;
+            }
+            if (n_items > 16 * slots) break;  // shorter slices only add set-up from here on
+        }
     }
 
     std::vector<WorkItem> items;
@@ -464,7 +534,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
                                  rw.new_row_base, rw.own_pos, 0, 0, 0});
                 continue;
             }
-            if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_items)
+            if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_slots)
                 return fail(PGQA_ERR_CAPACITY, "split partials exceed the plan capacity");
             for (int64_t s = 0; s < ns; ++s)
                 items.push_back({rw.page_base, static_cast<int32_t>(s * len),
@@ -484,6 +554,58 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
     });
 
+    // Prefill key slices: enough CTAs for about two per SM (each slice >= 256 keys, at
+    // most 8), partials merged per (row, kv head) like split decode rows.
+    int pf_splits = 1;
+    if (!prefill.empty()) {
+        int64_t kmax = 0;
+        for (const PrefillItem &t : prefill) kmax = std::max<int64_t>(kmax, t.key_end);
+        if (c.prefill_splits > 0)
+            pf_splits = std::min(8, c.prefill_splits);
+        else  // the most slices that still fit one wave of two CTAs per SM
+            pf_splits = static_cast<int>(std::min<int64_t>(
+                {8, std::max<int64_t>(1, 2LL * plan->num_sms / static_cast<int64_t>(prefill.size())),
+                 std::max<int64_t>(1, kmax / 256)}));
+    }
+    if (pf_splits > 1) {
+        // partial slots per (request, kv head): rows x splits, after the decode slots
+        std::vector<PrefillItem> split_items;
+        split_items.reserve(prefill.size() * pf_splits);
+        int64_t prev_req_key = -1, base = 0;
+        for (const PrefillItem &t : prefill) {
+            const int64_t req_key = (static_cast<int64_t>(t.q_row0) << 8) | t.kv_head;
+            if (req_key != prev_req_key) {
+                base = slot;
+                slot += t.rows * pf_splits;
+                if (slot > plan->max_slots) return fail(PGQA_ERR_CAPACITY, "split partials exceed the plan capacity");
+                for (int i = 0; i < t.rows; ++i) {
+                    if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks)
+                        return fail(PGQA_ERR_CAPACITY, "merge tasks exceed the plan capacity");
+                    tasks.push_back({t.q_row0 + i, t.kv_head, static_cast<int32_t>(base + i * pf_splits), pf_splits});
+                }
+                prev_req_key = req_key;
+            }
+            const int64_t len = round_up(ceil_div(std::max<int32_t>(1, t.key_end), pf_splits), 64);
+            for (int sidx = 0; sidx < pf_splits; ++sidx) {
+                PrefillItem u = t;
+                u.key_begin = static_cast<int32_t>(std::min<int64_t>(t.key_end, sidx * len));
+                u.key_end = static_cast<int32_t>(std::min<int64_t>(t.key_end, (sidx + 1) * len));
+                u.part_base = static_cast<int32_t>(base);
+                u.split = sidx;
+                u.num_splits = pf_splits;
+                split_items.push_back(u);
+            }
+        }
+        prefill.swap(split_items);
+        max_task_splits = std::max(max_task_splits, pf_splits);
+    }
+    if (static_cast<int64_t>(prefill.size()) > plan->max_prefill)
+        return fail(PGQA_ERR_CAPACITY, "prefill tiles exceed the plan capacity %d", plan->max_prefill);
+    // Longest prefill slices first.
+    std::stable_sort(prefill.begin(), prefill.end(), [](const PrefillItem &a, const PrefillItem &b) {
+        return a.key_end - a.key_begin > b.key_end - b.key_begin;
+    });
+
     // Stage in pinned memory (double-buffered) and copy into the persistent buffer.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int buf = plan->cur;
@@ -496,11 +618,17 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     const size_t items_bytes = sizeof(WorkItem) * items.size();
     const size_t tasks_off = sizeof(WorkItem) * plan->max_items;
     const size_t tasks_bytes = sizeof(MergeTask) * tasks.size();
+    const size_t prefill_off = plan->prefill_offset();
+    const size_t prefill_bytes = sizeof(PrefillItem) * prefill.size();
     if (items_bytes) std::memcpy(h, items.data(), items_bytes);
     if (tasks_bytes) std::memcpy(h + tasks_off, tasks.data(), tasks_bytes);
+    if (prefill_bytes) std::memcpy(h + prefill_off, prefill.data(), prefill_bytes);
     if (items_bytes) e = cudaMemcpyAsync(plan->d_meta, h, items_bytes, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess && tasks_bytes)
         e = cudaMemcpyAsync(static_cast<char *>(plan->d_meta) + tasks_off, h + tasks_off, tasks_bytes,
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && prefill_bytes)
+        e = cudaMemcpyAsync(static_cast<char *>(plan->d_meta) + prefill_off, h + prefill_off, prefill_bytes,
                             cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaEventRecord(plan->staged[buf], st);
     if (e != cudaSuccess) return cuda_fail(e, "work list upload");
@@ -516,6 +644,8 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         plan->stages = longest_item <= 3LL * kDecodeWarps * tile ? 3 : 2;
     }
     plan->n_items = static_cast<int>(items.size());
+    plan->n_prefill = static_cast<int>(prefill.size());
+    plan->causal = causal != 0;
     plan->n_tasks = static_cast<int>(tasks.size());
     plan->split_tokens = static_cast<int>(ls);
     plan->max_splits_used = max_used;
@@ -550,7 +680,7 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     } else if (flags & PGQA_RUN_POOL_STABLE) {
         return fail(PGQA_ERR_INVALID_ARG, "PGQA_RUN_POOL_STABLE applies to pgqa_append_run");
     }
-    if (plan->n_items == 0) return PGQA_OK;
+    if (plan->n_items == 0 && plan->n_prefill == 0) return PGQA_OK;
     if (!q || !k_pool || !v_pool || !out) return fail(PGQA_ERR_INVALID_ARG, "NULL tensor");
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return fail(PGQA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
@@ -561,12 +691,46 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     unsigned int *dflags = nullptr;
     pgqa_status s = device_flags(&dflags);
     if (s != PGQA_OK) return s;
+    const bool swz = plan->kernel == PGQA_DECODE_TENSOR_CORE;
     const CUtensorMap *mk = nullptr, *mv = nullptr;
-    s = pool_map(plan, k_pool, &mk);
-    if (s == PGQA_OK) s = pool_map(plan, v_pool, &mv);
+    s = pool_map(plan, k_pool, plan->box_rows, swz, &mk);
+    if (s == PGQA_OK) s = pool_map(plan, v_pool, plan->box_rows, swz, &mv);
     if (s != PGQA_OK) return s;
 
     const float scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(c.head_dim));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (plan->n_prefill > 0) {
+        const int prows = std::min(c.page_size, 64);
+        const CUtensorMap *pk = nullptr, *pv = nullptr;
+        s = pool_map(plan, k_pool, prows, true, &pk);
+        if (s == PGQA_OK) s = pool_map(plan, v_pool, prows, true, &pv);
+        if (s != PGQA_OK) return s;
+        PrefillParams pp{};
+        pp.q = q;
+        pp.items = plan->prefill_items();
+        pp.kv_indices = plan->kv_indices;
+        pp.num_pages = plan->num_pages;
+        pp.page_size = c.page_size;
+        pp.box_rows = prows;
+        pp.num_qo_heads = c.num_qo_heads;
+        pp.num_kv_heads = c.num_kv_heads;
+        pp.causal = plan->causal ? 1 : 0;
+        pp.scale_log2 = scale * 1.4426950408889634f;
+        pp.out = out;
+        pp.out_dtype = out_dtype;
+        pp.lse = lse;
+        pp.flags = dflags;
+        pp.k_new = k_new;
+        pp.v_new = v_new;
+        pp.k_pool = k_pool;
+        pp.v_pool = v_pool;
+        pp.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
+        pp.partial_o = plan->d_partial_o;
+        pp.partial_lse = plan->d_partial_lse;
+        e = launch_prefill(c.head_dim, plan->group, c.dtype, *pk, *pv, pp, plan->n_prefill, true, st);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    }
+    if (plan->n_items > 0) {
     DecodeParams p{};
     p.q = q;
     p.items = plan->items();
@@ -588,10 +752,12 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.v_pool = v_pool;
     p.num_kv_heads = c.num_kv_heads;
     p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // With a prefill grid just launched, the decode grid runs beside it.
+    p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,
                       true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    }
     if (plan->n_tasks > 0) {
         MergeParams mp{};
         mp.tasks = plan->tasks();

@@ -41,6 +41,25 @@ struct alignas(16) MergeTask {
 };
 static_assert(sizeof(MergeTask) == 16, "MergeTask is 16 bytes");
 
+// One CTA of the prefill-segment kernel: 64 (row, head) pairs of one kv head of
+// a multi-row request, pairs numbered m = i * G + h (i: row within the request).
+struct alignas(16) PrefillItem {
+    int32_t page_base;   // kv_indptr[request]
+    int32_t key_begin;   // key slice [key_begin, key_end) of this CTA (key_begin a multiple of 64)
+    int32_t key_end;
+    int32_t q_row0;      // first query row of the request
+    int32_t rows;        // L: query rows of the request
+    int32_t n_keys;      // N: keys of the request
+    int32_t kv_head;
+    int32_t pair0;       // first pair of the CTA
+    int32_t part_base;   // < 0: write final rows; else partial slot of (row i, split s) is
+                         // part_base + i * num_splits + s
+    int32_t split;       // s
+    int32_t num_splits;
+    int32_t pad;
+};
+static_assert(sizeof(PrefillItem) == 48, "PrefillItem is 48 bytes");
+
 // Warp tile (tokens one warp owns per pipeline stage) of the decode kernel.
 __host__ __device__ constexpr int decode_warp_tile(int head_dim) { return head_dim == 64 ? 32 : 16; }
 constexpr int kDecodeWarps = 4;
@@ -70,6 +89,33 @@ struct DecodeParams {
     int num_kv_heads;
     int prefetch_pool;         // 1: the pool rows (other than the new ones) are stable, so
                                // K/V loads may start before the grid-dependency wait
+    int defer_wait;            // 1: launched right after an independent prefill grid of the same
+                               // call; every older kernel is complete, so the dependency wait
+                               // moves to the end (it only keeps completion order)
+};
+
+struct PrefillParams {
+    const void *q;
+    const PrefillItem *items;
+    const int32_t *kv_indices;
+    int64_t num_pages;
+    int page_size;
+    int box_rows;              // rows per TMA box: min(page_size, 64)
+    int num_qo_heads;
+    int num_kv_heads;
+    int causal;                // bottom-right causal bound per row
+    float scale_log2;
+    void *out;
+    int out_dtype;
+    float *lse;
+    unsigned int *flags;
+    const void *k_new;         // fused append (nullable), as in DecodeParams
+    const void *v_new;
+    void *k_pool;
+    void *v_pool;
+    int prefetch_pool;
+    float *partial_o;          // split prefill rows: [slots, G, D]
+    float *partial_lse;        // [slots, G] log2 domain
 };
 
 struct MergeParams {
@@ -88,6 +134,9 @@ struct MergeParams {
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items,
                           bool pdl, cudaStream_t stream);
+cudaError_t launch_prefill(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+                           const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
+                           cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,
                          cudaStream_t stream);
 cudaError_t launch_kv_append(void *k_pool, void *v_pool, const void *k, const void *v,

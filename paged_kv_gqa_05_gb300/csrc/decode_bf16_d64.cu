@@ -3,6 +3,7 @@
 // CUDA-core kernel (groups 1..8).
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
+#include "prefill_tc.cuh"
 
 namespace pgqa {
 cudaError_t launch_decode_bf16_d64(int kind, int stages, int group, const CUtensorMap &tm_k,
@@ -11,5 +12,10 @@ cudaError_t launch_decode_bf16_d64(int kind, int stages, int group, const CUtens
     if (kind == PGQA_DECODE_CUDA_CORE)
         return launch_decode_dt<64, __nv_bfloat16>(group, tm_k, tm_v, p, num_items, pdl, stream);
     return launch_decode_tc<64, __nv_bfloat16>(stages, group, tm_k, tm_v, p, num_items, pdl, stream);
+}
+
+cudaError_t launch_prefill_bf16_d64(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const PrefillParams &p, int num_items, bool pdl, cudaStream_t stream) {
+    return launch_prefill_tc<64, __nv_bfloat16>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa

@@ -3,6 +3,7 @@
 // CUDA-core kernel (groups 1..8).
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
+#include "prefill_tc.cuh"
 
 namespace pgqa {
 cudaError_t launch_decode_fp16_d128(int kind, int stages, int group, const CUtensorMap &tm_k,
@@ -11,5 +12,10 @@ cudaError_t launch_decode_fp16_d128(int kind, int stages, int group, const CUten
     if (kind == PGQA_DECODE_CUDA_CORE)
         return launch_decode_dt<128, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
     return launch_decode_tc<128, __half>(stages, group, tm_k, tm_v, p, num_items, pdl, stream);
+}
+
+cudaError_t launch_prefill_fp16_d128(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                      const PrefillParams &p, int num_items, bool pdl, cudaStream_t stream) {
+    return launch_prefill_tc<128, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa

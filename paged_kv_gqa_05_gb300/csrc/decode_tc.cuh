@@ -200,14 +200,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     // K/V loads start before the grid-dependency wait when the caller has stated
     // that nothing still in flight writes the pool rows this call reads.
     const int pre = my_tiles < C::ST ? my_tiles : C::ST;
-    if (p.prefetch_pool && lane == 0)
-        for (int k = 0; k < pre; ++k) issue(k);
-    pdl_wait();
-    // Our predecessors are complete from here on, so a grid launched early after
-    // this trigger never overlaps a kernel older than this one.
-    pdl_launch_dependents();
-    if (!p.prefetch_pool && lane == 0)
-        for (int k = 0; k < pre; ++k) issue(k);
+    if (p.defer_wait) {
+        // Our predecessor is the prefill grid of the same call, which writes nothing
+        // we read and started only after everything older completed.
+        if (lane == 0)
+            for (int k = 0; k < pre; ++k) issue(k);
+    } else {
+        if (p.prefetch_pool && lane == 0)
+            for (int k = 0; k < pre; ++k) issue(k);
+        pdl_wait();
+        // Our predecessors are complete from here on, so a grid launched early after
+        // this trigger never overlaps a kernel older than this one.
+        pdl_launch_dependents();
+        if (!p.prefetch_pool && lane == 0)
+            for (int k = 0; k < pre; ++k) issue(k);
+    }
 
     // Q^T fragments (B operand): b0 = q[head g8][16ks + 2c4, +1], b1 = same + 8.
     // Heads >= G are zero columns.
@@ -431,6 +438,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     }
     constexpr int OS = C::OS;
     auto state = [&](int w) { return reinterpret_cast<float *>(pipe + w * C::ST * C::STAGE_BYTES); };
+    if (p.defer_wait) {
+        // Completion order: this grid finishes only after the prefill grid before it.
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     if (warp != 0) {
         float *st = state(warp);  // [8] m, [8] l, [8][OS] O
         if (g8 == 0) {

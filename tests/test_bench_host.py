@@ -1,0 +1,71 @@
+"""CPU tests of bench.py's host logic: the multi-rank plumbing (world size 2 over
+gloo: barrier, max/sum over ranks, rank-0-only reporting) and the reference arm
+(the CPU oracle) JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    r, w, local = bench.dist_env()
+    assert (r, w, local) == (rank, world, rank)
+    bench.init_dist(w, "gloo")
+    bench.barrier(w)
+    mx = bench.max_over_ranks(1.5 + rank, w)
+    sm = bench.sum_over_ranks(10.0 * (rank + 1), w)
+    ref = bench.run_reference(bench.main.__globals__["argparse"].Namespace(
+        steps=3, warmup=3, workload="tiny", seed=0), r, w)
+    q.put((rank, mx, sm, ref is None))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_rank_reductions_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == (0, 2.5, 30.0, False)   # rank 0 times the oracle
+    assert got[1] == (1, 2.5, 30.0, True)    # other ranks do no reference work
+
+
+def test_reference_arm_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                          "--warmup", "3", "--workload", "tiny"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["higher_is_better"] is True and line["steps"] == 3
+
+
+def test_warmup_floor():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0 and "warmup" in out.stderr

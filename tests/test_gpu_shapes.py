@@ -72,3 +72,22 @@ def test_explicit_scale():
     out = plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out_dtype=torch.float32, lse=lse,
                    sm_scale=0.3)
     H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "scale 0.3")
+
+
+@pytest.mark.parametrize("group,head_dim,page_size,dtype",
+                         [(7, 64, 64, "bf16"), (6, 128, 256, "fp16"), (1, 64, 16, "bf16"), (8, 128, 32, "bf16"),
+                          (3, 64, 128, "fp16"), (5, 128, 16, "bf16")])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_segments(group, head_dim, page_size, dtype, causal):
+    """Chunks of query rows (tensor-core prefill tiles) mixed with decode rows,
+    chunk lengths not multiples of 64 / G, plus a chunk longer than its history
+    (its first rows have no admissible key under the causal mask)."""
+    hkv = 2 if group <= 4 else 1
+    lens = [300, 5, 1030, 77, 3]
+    qo = [70, 1, 200, 77, 5]
+    w = W.custom("pf", lens, page_size, group * hkv, hkv, head_dim, dtype, 128, seed=group + head_dim,
+                 qo_lens=qo, causal=causal)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, info = H.gpu_outputs(w)
+    assert info["num_prefill_tiles"] > 0
+    H.compare(out, lse, ro, rl, f"prefill g{group} d{head_dim} ps{page_size} {dtype} causal={causal}")
