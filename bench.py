@@ -265,7 +265,7 @@ def run_ours(args, rank, world, local):
     plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dt, max_batch=w.batch,
                    max_q_rows=w.rows, max_splits=args.max_splits, split_tokens=args.split_tokens,
                    ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel,
-                   pipeline_stages=args.stages)
+                   pipeline_stages=args.stages, decode_ctas=args.decode_ctas)
     stream = torch.cuda.Stream(device)
     launches_per_layer = {}
 
@@ -529,6 +529,8 @@ def main(argv=None):
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto")
     ap.add_argument("--stages", type=int, default=0, choices=[0, 2, 3], help="pipeline stages per warp")
+    ap.add_argument("--decode-ctas", type=int, default=0,
+                    help="0: one CTA per work item; n: n persistent CTAs; -1: one persistent CTA per SM")
     ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -126,6 +126,9 @@ typedef struct pgqa_plan_config {
     int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
                              per plan_update (3 when a whole slice fits in flight, else 2) */
     int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
+    int decode_ctas;      /* tensor-core decode: 0 = one CTA per work item (the default);
+                             n > 0 = n persistent CTAs walking the work list; -1 = one
+                             persistent CTA per SM */
 } pgqa_plan_config;
 
 #define PGQA_DECODE_AUTO 0

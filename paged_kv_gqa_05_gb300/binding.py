@@ -45,7 +45,8 @@ class PlanConfig(ctypes.Structure):
                 ("max_batch", ctypes.c_int), ("max_q_rows", ctypes.c_int64),
                 ("max_splits", ctypes.c_int), ("split_tokens", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("decode_kernel", ctypes.c_int),
-                ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int)]
+                ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
+                ("decode_ctas", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -162,13 +163,13 @@ def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: to
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
-                pipeline_stages: int = 0, prefill_splits: int = 0) -> int:
+                pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0) -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
     decode_kernel: "auto" | "tensor_core" | "cuda_core"."""
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
     cfg = PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                      max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
-                     pipeline_stages, prefill_splits)
+                     pipeline_stages, prefill_splits, decode_ctas)
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value

@@ -16,18 +16,18 @@
 
 namespace pgqa {
 using DecodeLauncher = cudaError_t (*)(int, int, int, const CUtensorMap &, const CUtensorMap &,
-                                        const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+                                        const DecodeParams &, int, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
 
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, int grid, bool pdl,
                           cudaStream_t stream) {
     DecodeLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_decode_bf16_d64 : launch_decode_bf16_d128)
                                           : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
-    return f(kind, stages, group, tm_k, tm_v, p, num_items, pdl, stream);
+    return f(kind, stages, group, tm_k, tm_v, p, num_items, grid, pdl, stream);
 }
 using PrefillLauncher = cudaError_t (*)(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int,
                                          bool, cudaStream_t);
@@ -319,6 +319,7 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
     if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
         return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
+    if (c.decode_ctas < -1) return fail(PGQA_ERR_INVALID_ARG, "decode_ctas %d", c.decode_ctas);
     if (c.prefill_splits < 0 || c.prefill_splits > 8)
         return fail(PGQA_ERR_INVALID_ARG, "prefill_splits %d (0..8)", c.prefill_splits);
     if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
@@ -754,8 +755,11 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
     // With a prefill grid just launched, the decode grid runs beside it.
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
+    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0)
+                         ? (c.decode_ctas > 0 ? c.decode_ctas : plan->num_sms)
+                         : 0;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,
-                      true, st);
+                      grid, true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     }
     if (plan->n_tasks > 0) {

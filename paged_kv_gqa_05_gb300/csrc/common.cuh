@@ -131,8 +131,10 @@ struct MergeParams {
 };
 
 // Launchers (defined in the kernel translation units).
+// grid > 0: persistent tensor-core kernel with that many CTAs walking the work list;
+// grid <= 0: one CTA per work item.
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items,
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, int grid,
                           bool pdl, cudaStream_t stream);
 cudaError_t launch_prefill(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                            const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
@@ -298,6 +300,31 @@ __device__ __forceinline__ void named_bar_arrive(int count) {
 }
 __device__ __forceinline__ void named_bar_sync(int count) {
     asm volatile("bar.sync 1, %0;" ::"r"(count) : "memory");
+}
+// Named barrier with a compile-time id (a runtime id would reserve all sixteen).
+template <int ID>
+__device__ __forceinline__ void named_bar_arrive_c(int count) {
+    asm volatile("bar.arrive %0, %1;" ::"n"(ID), "r"(count) : "memory");
+}
+template <int ID>
+__device__ __forceinline__ void named_bar_sync_c(int count) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive_id(int id, int count) {
+    switch (id) {
+        case 1: named_bar_arrive_c<1>(count); break;
+        case 2: named_bar_arrive_c<2>(count); break;
+        case 3: named_bar_arrive_c<3>(count); break;
+        default: named_bar_arrive_c<4>(count); break;
+    }
+}
+__device__ __forceinline__ void named_bar_sync_id(int id, int count) {
+    switch (id) {
+        case 1: named_bar_sync_c<1>(count); break;
+        case 2: named_bar_sync_c<2>(count); break;
+        case 3: named_bar_sync_c<3>(count); break;
+        default: named_bar_sync_c<4>(count); break;
+    }
 }
 
 // 16-byte shared-memory load through a plain C++ access, so the compiler orders

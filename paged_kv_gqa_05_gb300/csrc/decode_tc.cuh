@@ -429,7 +429,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
 
     // ---- combine the warps.  Per head column: M = max_w m_w, L = sum_w l_w 2^(m_w - M),
     // O = sum_w 2^(m_w - M) O_w / L.  Each warp leaves (m, l, O) in its own stage area
-    // (its TMA copies have all landed) and warps 1.. exit; warp 0 combines.
+    // (its TMA copies have all landed); after one CTA barrier every thread builds 8
+    // output channels of one head.
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
@@ -438,12 +439,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     }
     constexpr int OS = C::OS;
     auto state = [&](int w) { return reinterpret_cast<float *>(pipe + w * C::ST * C::STAGE_BYTES); };
-    if (p.defer_wait) {
-        // Completion order: this grid finishes only after the prefill grid before it.
-        pdl_wait();
-        pdl_launch_dependents();
-    }
-    if (warp != 0) {
+    {
         float *st = state(warp);  // [8] m, [8] l, [8][OS] O
         if (g8 == 0) {
             st[2 * c4] = m_run[0];
@@ -459,89 +455,67 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
             ow[8] = o[dt][2];
             ow[OS + 8] = o[dt][3];
         }
-        named_bar_arrive(C::NW * 32);
-        return;
     }
-    named_bar_sync(C::NW * 32);
+    if (p.defer_wait) {
+        // Completion order: this grid finishes only after the prefill grid before it.
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    __syncthreads();
 
-    float f[C::NW][2], lse2[2];
+    constexpr int CH8 = D / 8;
+    for (int idx = threadIdx.x; idx < G * CH8; idx += C::NW * 32) {
+        const int h = idx / CH8;
+        const int c8 = (idx - h * CH8) * 8;
+        float mw[C::NW], Mx = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int hh = 2 * c4 + h;
-        float Mx = m_run[h];
+        for (int w = 0; w < C::NW; ++w) {
+            mw[w] = state(w)[h];
+            Mx = fmaxf(Mx, mw[w]);
+        }
+        float fw[C::NW], L = 0.f;
 #pragma unroll
-        for (int w = 1; w < C::NW; ++w) Mx = fmaxf(Mx, state(w)[hh]);
-        float L = (m_run[h] == -INFINITY) ? 0.f : l_run[h] * ex2_approx(m_run[h] - Mx);
-#pragma unroll
-        for (int w = 1; w < C::NW; ++w) {
-            const float mw = state(w)[hh];
-            if (mw != -INFINITY) L += state(w)[8 + hh] * ex2_approx(mw - Mx);
+        for (int w = 0; w < C::NW; ++w) {
+            fw[w] = (mw[w] == -INFINITY) ? 0.f : ex2_approx(mw[w] - Mx);
+            L += state(w)[8 + h] * fw[w];
         }
         // L == 0 only when no key was admissible; a NaN (poisoned row) propagates.
         const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
-        f[0][h] = (m_run[h] == -INFINITY) ? 0.f : ex2_approx(m_run[h] - Mx) * inv;
+        float acc[8];
 #pragma unroll
-        for (int w = 1; w < C::NW; ++w) {
-            const float mw = state(w)[hh];
-            f[w][h] = (mw == -INFINITY) ? 0.f : ex2_approx(mw - Mx) * inv;
+        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::NW; ++w) {
+            const float4 a = *reinterpret_cast<const float4 *>(state(w) + 16 + h * OS + c8);
+            const float4 b = *reinterpret_cast<const float4 *>(state(w) + 16 + h * OS + c8 + 4);
+            const float f = fw[w] * inv;
+            acc[0] += a.x * f; acc[1] += a.y * f; acc[2] += a.z * f; acc[3] += a.w * f;
+            acc[4] += b.x * f; acc[5] += b.y * f; acc[6] += b.z * f; acc[7] += b.w * f;
         }
-        lse2[h] = (L == 0.f) ? -INFINITY : Mx + lg2_approx(L);
-    }
-    float *fin = state(0) + 16;  // [8][OS] final O of this slice, staged for vector stores
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int h = j & 1;
-            const int off = (2 * c4 + h) * OS + dt * 16 + g8 + (j >> 1) * 8;
-            float acc = o[dt][j] * f[0][h];
-#pragma unroll
-            for (int w = 1; w < C::NW; ++w) acc += state(w)[16 + off] * f[w][h];
-            fin[off] = acc;
-        }
-    }
-    __syncwarp();
-
-    constexpr int CH8 = D / 8;
-    for (int idx = lane; idx < G * CH8; idx += 32) {
-        const int h = idx / CH8;
-        const int c8 = (idx - h * CH8) * 8;
-        const float4 a = *reinterpret_cast<const float4 *>(fin + h * OS + c8);
-        const float4 b = *reinterpret_cast<const float4 *>(fin + h * OS + c8 + 4);
+        const float lse2 = (L == 0.f) ? -INFINITY : Mx + lg2_approx(L);
         const int head = it.kv_head * G + h;
         if (it.out_slot < 0) {
             const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c8;
             if (p.out_dtype == PGQA_FP32) {
                 float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + oi);
-                dst[0] = a;
-                dst[1] = b;
+                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
             } else {
                 uint4 v;
-                v.x = M::pack(a.x, a.y);
-                v.y = M::pack(a.z, a.w);
-                v.z = M::pack(b.x, b.y);
-                v.w = M::pack(b.z, b.w);
+                v.x = M::pack(acc[0], acc[1]);
+                v.y = M::pack(acc[2], acc[3]);
+                v.z = M::pack(acc[4], acc[5]);
+                v.w = M::pack(acc[6], acc[7]);
                 *reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + oi) = v;
             }
+            if (c8 == 0 && p.lse != nullptr)
+                p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = lse2 * 0.6931471805599453f;
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.partial_o + (static_cast<size_t>(it.out_slot) * G + h) * D + c8);
-            dst[0] = a;
-            dst[1] = b;
-        }
-    }
-    if (g8 == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int hh = 2 * c4 + h;
-            if (hh < G) {
-                const int head = it.kv_head * G + hh;
-                if (it.out_slot < 0) {
-                    if (p.lse != nullptr)
-                        p.lse[static_cast<size_t>(it.q_row) * p.num_qo_heads + head] = lse2[h] * 0.6931471805599453f;
-                } else {
-                    p.partial_lse[static_cast<size_t>(it.out_slot) * G + hh] = lse2[h];
-                }
-            }
+            const size_t slot = static_cast<size_t>(it.out_slot) * G + h;
+            float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D + c8);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (c8 == 0) p.partial_lse[slot] = lse2;
         }
     }
 }

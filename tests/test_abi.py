@@ -48,7 +48,7 @@ def test_status_strings(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks behaviour without a device")
 def test_no_device_gives_cuda_status(lib):
     from paged_kv_gqa_05_gb300 import binding
-    cfg = binding.PlanConfig(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0)
+    cfg = binding.PlanConfig(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0)
     h = ctypes.c_void_p()
     assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)) == 4
     assert h.value is None
@@ -57,7 +57,7 @@ def test_no_device_gives_cuda_status(lib):
 
 def test_argument_checks_before_device(lib):
     # shape checks fire before any CUDA call, so they work without a GPU
-    cfg_bad = __import__("paged_kv_gqa_05_gb300").binding.PlanConfig(14, 2, 96, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0)
+    cfg_bad = __import__("paged_kv_gqa_05_gb300").binding.PlanConfig(14, 2, 96, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0)
     h = ctypes.c_void_p()
     assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg_bad)) == 2
     assert lib.pgqa_kv_append(None, None, 1, 16, 2, 64, 0, None, None, None, 0, None) == 0

@@ -17,6 +17,9 @@ LENS = [0, 1, 5, 16, 17, 31, 33, 100, 257, 700]
 
 
 KERNELS = ["tensor_core", "cuda_core"]
+# tensor-core decode schedules: persistent (one CTA per SM), a tiny persistent grid (many
+# items per CTA), and one CTA per work item
+SCHEDULES = {"per_item": {}, "grid3": {"decode_ctas": 3}, "persistent": {"decode_ctas": -1}}
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -27,6 +30,16 @@ def test_page_sizes(page_size, head_dim, kernel):
     for opts in ({}, {"split_tokens": 32}, {"max_splits": 1}):
         out, lse, _ = H.gpu_outputs(w, decode_kernel=kernel, **opts)
         H.compare(out, lse, ro, rl, f"{kernel}/ps{page_size}/d{head_dim}/{opts}")
+
+
+@pytest.mark.parametrize("schedule", sorted(SCHEDULES))
+@pytest.mark.parametrize("head_dim,dtype", [(64, "bf16"), (128, "fp16")])
+def test_decode_schedules(schedule, head_dim, dtype):
+    w = W.custom("sched", LENS * 3, 16, 14, 2, head_dim, dtype, 512, seed=head_dim + 5)
+    ro, rl = H.oracle_outputs(w)
+    for opts in ({}, {"split_tokens": 32}):
+        out, lse, _ = H.gpu_outputs(w, **SCHEDULES[schedule], **opts)
+        H.compare(out, lse, ro, rl, f"{schedule}/d{head_dim}/{opts}")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
