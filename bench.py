@@ -36,7 +36,7 @@ import torch  # noqa: E402
 
 METRIC = "paged GQA decode: achieved HBM GB/s (% of peak); µs/layer call at 128x300 ctx"
 LAYERS = {"qwen05_decode": 24, "qwen15_mixed": 28, "long_context_b1": 8, "long_context_b4": 3,
-          "ragged": 4, "tiny": 1}
+          "ragged": 4, "wide_group": 4, "tiny": 1}
 FALLBACK_HBM_GBS = 6800.0
 
 

@@ -23,7 +23,9 @@
  *       lse       [total_q_rows, num_qo_heads]  fp32, natural log
  *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads).
  *   - Supported shapes: head_dim 64 or 128; page_size 16, 32, 64, 128 or 256;
- *     num_qo_heads / num_kv_heads between 1 and 8; bf16 or fp16 q/k/v.
+ *     num_qo_heads / num_kv_heads between 1 and 16 (1 and 8 for the CUDA-core
+ *     decode kernel, the persistent decode schedule and
+ *     pgqa_decode_static_scratch); bf16 or fp16 q/k/v.
  *     Anything else returns PGQA_ERR_UNSUPPORTED.
  *   - Pool, q, k, v and out pointers must be 16-byte aligned.
  */
@@ -120,7 +122,8 @@ typedef struct pgqa_plan_config {
     int max_splits;       /* cap on slices per (request, kv head); 0 = no cap; 1 = never split */
     int split_tokens;     /* > 0 forces this slice length (rounded up to the kernel tile);
                              0 = choose it so that the slices fill the SMs */
-    int ctas_per_sm;      /* occupancy target of the split heuristic; 0 = library default */
+    int ctas_per_sm;      /* CTA slots per SM assumed by the split heuristic; 0 = the decode
+                             kernel's resident CTAs per SM, at most 2 */
     int decode_kernel;    /* PGQA_DECODE_AUTO (tensor cores), PGQA_DECODE_TENSOR_CORE or
                              PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
     int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
@@ -128,7 +131,8 @@ typedef struct pgqa_plan_config {
     int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
     int decode_ctas;      /* tensor-core decode: 0 = one CTA per work item (the default);
                              n > 0 = n persistent CTAs walking the work list; -1 = one
-                             persistent CTA per SM */
+                             persistent CTA per SM.  Groups wider than 8 heads always run
+                             one CTA per item. */
 } pgqa_plan_config;
 
 #define PGQA_DECODE_AUTO 0

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -28,6 +29,17 @@ cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dt
     DecodeLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_decode_bf16_d64 : launch_decode_bf16_d128)
                                           : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
     return f(kind, stages, group, tm_k, tm_v, p, num_items, grid, pdl, stream);
+}
+cudaError_t decode_blocks_per_sm_bf16_d64(int, int, int *);
+cudaError_t decode_blocks_per_sm_bf16_d128(int, int, int *);
+cudaError_t decode_blocks_per_sm_fp16_d64(int, int, int *);
+cudaError_t decode_blocks_per_sm_fp16_d128(int, int, int *);
+
+// Resident CTAs per SM of the per-item tensor-core decode kernel for (stages, group).
+cudaError_t decode_blocks_per_sm(int stages, int head_dim, int group, pgqa_dtype dtype, int *blocks) {
+    auto f = dtype == PGQA_BF16 ? (head_dim == 64 ? decode_blocks_per_sm_bf16_d64 : decode_blocks_per_sm_bf16_d128)
+                                : (head_dim == 64 ? decode_blocks_per_sm_fp16_d64 : decode_blocks_per_sm_fp16_d128);
+    return f(stages, group, blocks);
 }
 using PrefillLauncher = cudaError_t (*)(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int,
                                          bool, cudaStream_t);
@@ -157,7 +169,8 @@ struct pgqa_plan {
     int group = 0;
     int tile = 0;       // decode warp tile (tokens)
     int box_rows = 0;
-    int ctas_per_sm = 0;
+    int ctas_per_sm = 0;     // CTA slots per SM for 2-stage plans (the most of any variant)
+    int slots_per_sm[4] = {0, 0, 0, 0};  // by pipeline depth (2 or 3): resident decode CTAs per SM
     int kernel = PGQA_DECODE_TENSOR_CORE;
     int stages = 2;     // per-warp pipeline depth of the tensor-core kernel (chosen per plan_update)
     int max_items = 0;  // capacity of the work list and of the partial slots
@@ -309,7 +322,10 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "num_qo_heads %d must be a positive multiple of num_kv_heads %d",
                     c.num_qo_heads, c.num_kv_heads);
     const int group = c.num_qo_heads / c.num_kv_heads;
-    if (group > 8) return fail(PGQA_ERR_UNSUPPORTED, "query heads per kv head %d > 8", group);
+    // The tensor-core decode tile holds 16 heads (two n tiles); the CUDA-core kernel 8.
+    const int max_group = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? 8 : 16;
+    if (group > max_group)
+        return fail(PGQA_ERR_UNSUPPORTED, "query heads per kv head %d > %d", group, max_group);
     if (c.head_dim != 64 && c.head_dim != 128) return fail(PGQA_ERR_UNSUPPORTED, "head_dim %d", c.head_dim);
     if (!supported_page_size(c.page_size)) return fail(PGQA_ERR_UNSUPPORTED, "page_size %d", c.page_size);
     if (c.dtype != PGQA_BF16 && c.dtype != PGQA_FP16) return fail(PGQA_ERR_UNSUPPORTED, "dtype must be bf16/fp16");
@@ -331,16 +347,31 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->group = group;
     p->tile = decode_warp_tile(c.head_dim);
     p->box_rows = std::min(c.page_size, p->tile);
-    p->ctas_per_sm = c.ctas_per_sm > 0 ? c.ctas_per_sm : 2;
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
     p->stages = c.pipeline_stages == 3 ? 3 : 2;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    // CTA slots of the split heuristic, unless the caller fixes them: the resident CTAs
+    // per SM of the kernel that will run (registers and shared memory decide), at most
+    // two.  Timed on GB300, a third resident CTA adds no bandwidth once HBM is saturated
+    // and only shortens every slice (uniform 4 x 32768-token batch, d 128: 304 slices
+    // 26.3 us, 456 slices 28.8 us).
+    for (int st = 2; st <= 3 && e == cudaSuccess; ++st) {
+        int b = 2;  // the CUDA-core kernel's launch bound
+        if (c.ctas_per_sm > 0) {
+            b = c.ctas_per_sm;
+        } else if (p->kernel == PGQA_DECODE_TENSOR_CORE) {
+            e = decode_blocks_per_sm(st, c.head_dim, group, c.dtype, &b);
+            b = std::min(b, 2);
+        }
+        p->slots_per_sm[st] = std::max(1, b);
+    }
     if (e != cudaSuccess) {
         plan_free(p);
         return cuda_fail(e, "device query");
     }
-    // Slices never exceed (target CTAs) + (one per row and kv head); forced short slices may need more.
+    p->ctas_per_sm = std::max(p->slots_per_sm[2], p->slots_per_sm[3]);
+    // Slices never exceed 8 waves of CTAs + one per row and kv head; forced short slices may need more.
     const int64_t items = c.max_q_rows * c.num_kv_heads + 8LL * p->num_sms * p->ctas_per_sm + 64;
     if (items > (1 << 26)) {
         plan_free(p);
@@ -389,6 +420,119 @@ pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info) {
     return PGQA_OK;
 }
 
+// Admissible keys of one query row and where its new K/V rows go.
+struct Row {
+    int32_t q_row, page_base, n;  // n: admissible keys of the row
+    int32_t new_begin, new_row_base, own_pos;
+};
+
+// Streaming rate model of the per-item decode kernel on GB300, fitted to timed
+// launches of uniform and mixed batches (bytes per ns, i.e. GB/s):
+//   one CTA alone streams at kCtaRate (latency-bound: ~64 KB in flight per CTA with
+//   two stages, 1.4x that with three); n CTAs together at n c / (1 + (n c / P)^3)^(1/3),
+//   which saturates at P, the rate the kernel reaches with every slot busy.
+static double cta_rate(int head_dim, int group, int stages) {
+    const double c = head_dim == 64 ? 30.0 : (group <= 8 ? 40.0 : 35.0);
+    return stages == 3 ? 1.4 * c : c;
+}
+static constexpr double kSaturatedRate = 5300.0;  // bytes / ns
+static constexpr double kWaveCostNs = 1500.0;     // CTA set-up + epilogue, per wave of CTAs
+static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any row is split
+
+// Slice length (whole warp tiles, at least one tile per warp) for the decode rows that
+// minimises the estimated launch time.  The hardware runs `slots` CTAs at once and
+// starts the rest (longest first) as slots free up, so the estimate walks waves of
+// `slots` items: each wave takes max(its bytes / rate(CTAs in it), its longest slice /
+// one CTA's rate), plus kWaveCostNs; splitting adds kMergeCostNs.
+static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_rows, int64_t longest) {
+    const pgqa_plan_config &c = plan->cfg;
+    const int64_t tile = plan->tile;
+    const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
+    const double row_bytes = 4.0 * c.head_dim;  // K + V of one token of one kv head
+    // distinct admissible-key counts, longest first, with their multiplicity
+    std::vector<int64_t> lens(static_cast<size_t>(n_rows));
+    for (int64_t i = 0; i < n_rows; ++i) lens[i] = rows[i].n;
+    std::sort(lens.begin(), lens.end(), std::greater<int64_t>());
+    std::vector<std::pair<int64_t, int64_t>> hist;  // (n, rows)
+    for (int64_t n : lens) {
+        if (!hist.empty() && hist.back().first == n)
+            ++hist.back().second;
+        else
+            hist.push_back({n, 1});
+    }
+    std::vector<std::pair<int64_t, int64_t>> slices;  // (slice length, items)
+    slices.reserve(2 * hist.size());
+    int64_t best_len = round_up(std::max<int64_t>(longest, min_split), tile), prev_len = -1;
+    double best = 0.0;
+    bool have = false;
+    for (int64_t parts = 1;; ++parts) {
+        const int64_t len = round_up(ceil_div(std::max<int64_t>(1, longest), parts), tile);
+        if (len < min_split && have) break;
+        if (len == prev_len) continue;
+        prev_len = len;
+        slices.clear();
+        int64_t n_items = 0, max_slice = 0;
+        bool split = false;
+        for (const auto &h : hist) {
+            const int64_t n = h.first, cnt = h.second * c.num_kv_heads;
+            if (n == 0) {
+                slices.push_back({0, cnt});
+                n_items += cnt;
+                continue;
+            }
+            int64_t ns = ceil_div(n, std::max(len, min_split));
+            if (c.max_splits > 0) ns = std::min<int64_t>(ns, c.max_splits);
+            const int64_t sl = round_up(ceil_div(n, ns), tile);
+            ns = ceil_div(n, sl);
+            if (ns > 1) slices.push_back({sl, (ns - 1) * cnt});
+            slices.push_back({n - (ns - 1) * sl, cnt});
+            n_items += ns * cnt;
+            max_slice = std::max(max_slice, std::min(sl, n));
+            split = split || ns > 1;
+        }
+        const int stages = c.pipeline_stages != 0 ? c.pipeline_stages
+                                                  : (max_slice <= 3LL * kDecodeWarps * tile ? 3 : 2);
+        const int64_t slots = static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[stages];
+        if (have && (n_items > 8 * slots || n_items > plan->max_items)) break;
+        const double cr = cta_rate(c.head_dim, plan->group, stages);
+        std::sort(slices.begin(), slices.end(), std::greater<std::pair<int64_t, int64_t>>());
+        double t = 0.0, wave_bytes = 0.0;
+        int64_t free_slots = slots, in_wave = 0, first = -1;
+        auto close_wave = [&]() {
+            const double nc = static_cast<double>(in_wave) * cr;
+            const double rate = nc / std::cbrt(1.0 + std::pow(nc / kSaturatedRate, 3.0));
+            t += std::max(wave_bytes / rate, static_cast<double>(first) * row_bytes / cr) + kWaveCostNs;
+        };
+        for (const auto &sl : slices) {
+            int64_t cnt = sl.second;
+            while (cnt > 0) {
+                const int64_t take = std::min(cnt, free_slots);
+                if (first < 0) first = sl.first;
+                wave_bytes += static_cast<double>(take) * sl.first * row_bytes;
+                in_wave += take;
+                cnt -= take;
+                free_slots -= take;
+                if (free_slots == 0) {
+                    close_wave();
+                    free_slots = slots;
+                    wave_bytes = 0.0;
+                    in_wave = 0;
+                    first = -1;
+                }
+            }
+        }
+        if (in_wave > 0) close_wave();
+        if (split) t += kMergeCostNs;
+        if (!have || t < best) {
+            best = t;
+            best_len = len;
+            have = true;
+        }
+        if (len <= min_split) break;
+    }
+    return best_len;
+}
+
 pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
                              const int32_t *qo_indptr, int batch, const int32_t *kv_indices,
                              const int32_t *kv_indices_host, int64_t num_pages, int causal,
@@ -431,13 +575,9 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
                     static_cast<long long>(c.max_q_rows));
 
     // Admissible keys per query row (bottom-right causal for multi-row requests).
-    struct Row {
-        int32_t q_row, page_base, n;   // n: admissible keys of the row
-        int32_t new_begin, new_row_base, own_pos;
-    };
     std::vector<Row> rowv;
     rowv.reserve(static_cast<size_t>(rows));
-    int64_t work = 0, kv_tokens = 0;
+    int64_t kv_tokens = 0;
     bool fusable = true;
     std::vector<PrefillItem> prefill;
     for (int b = 0; b < batch; ++b) {
@@ -470,54 +610,14 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
             rowv.push_back({static_cast<int32_t>(r), kv_indptr[b], static_cast<int32_t>(a),
                             static_cast<int32_t>(nb), static_cast<int32_t>(L <= n ? r0 - nb : 0),
                             static_cast<int32_t>(L <= n ? nb + (r - r0) : -1)});
-            work += a;
         }
     }
-    work *= c.num_kv_heads;
 
     const int tile = plan->tile;
-    const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
-    int64_t ls;
     int64_t longest = 0;
     for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
-    if (c.split_tokens > 0) {
-        ls = round_up(c.split_tokens, tile);
-    } else {
-        // Pick the slice length (whole warp tiles, at least one tile per warp) that
-        // minimises a makespan estimate over num_sms * ctas_per_sm CTA slots, in bytes:
-        //   max(total / slots, longest slice) + per-CTA set-up x CTAs per slot
-        //   (+ the merge launch once any row is split).
-        // Uniform short rows stay whole; long rows are cut near the per-slot share.
-        const double slots = static_cast<double>(plan->num_sms) * plan->ctas_per_sm;
-        const double row_bytes = 4.0 * c.head_dim;  // K + V of one token of one kv head
-        const double cta_cost = 24.0 * 1024, merge_cost = 40.0 * 1024;
-        const double share = static_cast<double>(work) * row_bytes / slots;
-        const int64_t k_lo = min_split / tile;
-        const int64_t k_hi = std::max<int64_t>(k_lo, ceil_div(std::max<int64_t>(1, longest), tile));
-        double best = 0.0;
-        ls = k_hi * tile;
-        for (int64_t k = k_hi; k >= k_lo; --k) {
-            const int64_t len = k * tile;
-            int64_t n_items = 0, max_slice = 0;
-            bool split = false;
-            for (const Row &rw : rowv) {
-                int64_t ns = rw.n == 0 ? 1 : ceil_div(rw.n, len);
-                if (c.max_splits > 0) ns = std::min<int64_t>(ns, c.max_splits);
-                const int64_t sl = rw.n == 0 ? 0 : round_up(ceil_div(rw.n, ns), tile);
-                n_items += ns;
-                max_slice = std::max(max_slice, std::min<int64_t>(sl, rw.n));
-                split = split || ns > 1;
-            }
-            n_items *= c.num_kv_heads;
-            const double est = std::max(share, max_slice * row_bytes) + cta_cost * std::ceil(n_items / slots) +
-                               (split ? merge_cost : 0.0);
-            if (k == k_hi || est < best) {
-                best = est;
-                ls = len;
-            }
-            if (n_items > 16 * slots) break;  // shorter slices only add set-up from here on
-        }
-    }
+    const int64_t ls = c.split_tokens > 0 ? round_up(c.split_tokens, tile)
+                                          : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest);
 
     std::vector<WorkItem> items;
     std::vector<MergeTask> tasks;
@@ -755,7 +855,8 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
     // With a prefill grid just launched, the decode grid runs beside it.
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
-    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0)
+    // The persistent schedule serves groups of up to 8 heads; wider groups run one CTA per item.
+    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0 && plan->group <= 8)
                          ? (c.decode_ctas > 0 ? c.decode_ctas : plan->num_sms)
                          : 0;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,

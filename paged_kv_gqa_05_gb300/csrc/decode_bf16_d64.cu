@@ -1,5 +1,5 @@
 // Split-KV decode partial kernels instantiated for bf16, head_dim 64: the
-// tensor-core kernel (any group width up to 8; one CTA per work item with 2- or
+// tensor-core kernel (any group width up to 16; one CTA per work item with 2- or
 // 3-stage pipelines, or the persistent form), the CUDA-core kernel (groups 1..8) and
 // the prefill-segment kernel.
 #include "decode_simt.cuh"
@@ -15,6 +15,10 @@ cudaError_t launch_decode_bf16_d64(int kind, int stages, int group, const CUtens
         return launch_decode_dt<64, __nv_bfloat16>(group, tm_k, tm_v, p, num_items, pdl, stream);
     if (grid > 0) return launch_decode_tcp<64, __nv_bfloat16>(group, tm_k, tm_v, p, num_items, grid, pdl, stream);
     return launch_decode_tc<64, __nv_bfloat16>(stages, group, tm_k, tm_v, p, num_items, pdl, stream);
+}
+
+cudaError_t decode_blocks_per_sm_bf16_d64(int stages, int group, int *blocks) {
+    return decode_tc_blocks_per_sm<64, __nv_bfloat16>(stages, group, blocks);
 }
 
 cudaError_t launch_prefill_bf16_d64(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,

@@ -1,13 +1,14 @@
 // Split-KV paged GQA decode, tensor-core partial kernel (mma.sync m16n8k16).
 //
 // Same work decomposition as the CUDA-core kernel: one CTA per (query row, kv
-// head, key slice), serving the G <= 8 query heads that share the kv head, so
+// head, key slice), serving the G <= 16 query heads that share the kv head, so
 // every K/V row of the slice is read from HBM once for the whole group
 // ("A library kernel for decode", section "What changed", for the split-KV
 // scheme; the "flashlet" README's NHD pool layout for the addressing).
 //
 // The group is a dense tile in "swap-AB" form: tokens are the M dimension (16
-// per MMA), the G heads padded to 8 are N, head_dim is K.
+// per MMA), the G heads padded to 8 (one n tile) or 16 (two n tiles sharing
+// every K and V A-fragment) are N, head_dim is K.
 //   S^T[16 tok x 8 heads]  = K[16 tok x d]   . Q^T[d x 8 heads]     (fp32 accumulate)
 //   O^T[16 d   x 8 heads] += V^T[16 d x tok] . P^T[tok x 8 heads]
 // K comes from shared memory through ldmatrix, V through ldmatrix.trans; Q^T
@@ -102,9 +103,7 @@ struct TcCfg {
     static constexpr int DT = D / 16;                    // d m-tiles of the PV product
     static constexpr int KS = D / 16;                    // k-steps of the QK product
     static constexpr int OS = D + 4;                     // padded row stride (floats) of a warp's O
-    static constexpr int WARP_COMBINE_BYTES = (16 + 8 * OS) * 4;
     static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4;
-    static_assert(WARP_COMBINE_BYTES <= ST * STAGE_BYTES, "a warp's combine state fits its own stages");
     static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
 };
 
@@ -115,11 +114,13 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * (decode_warp_tile(D) * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, int STAGES, typename T>
-__global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
+template <int D, int STAGES, int NH, typename T>
+__global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 3 : 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p, int G) {
+    // NH tiles of 8 query heads: G <= 8 * NH (NH = 2 serves groups of 9..16 heads).
     using C = TcCfg<D, STAGES>;
+    constexpr int HP = 8 * NH;  // heads padded to whole n tiles
     using M = MmaType<T>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -218,16 +219,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
 
     // Q^T fragments (B operand): b0 = q[head g8][16ks + 2c4, +1], b1 = same + 8.
     // Heads >= G are zero columns.
-    uint32_t qf[C::KS][2];
-    {
-        const bool real = g8 < G;
+    uint32_t qf[C::KS][NH][2];
+#pragma unroll
+    for (int nh = 0; nh < NH; ++nh) {
+        const int hq = g8 + 8 * nh;
+        const bool real = hq < G;
         const T *qp = static_cast<const T *>(p.q) +
-                      (static_cast<size_t>(it.q_row) * p.num_qo_heads + it.kv_head * G + (real ? g8 : 0)) * D;
+                      (static_cast<size_t>(it.q_row) * p.num_qo_heads + it.kv_head * G + (real ? hq : 0)) * D;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
             const uint32_t *w = reinterpret_cast<const uint32_t *>(qp + ks * 16 + 2 * c4);
-            qf[ks][0] = real ? __ldg(w) : 0u;
-            qf[ks][1] = real ? __ldg(w + 4) : 0u;
+            qf[ks][nh][0] = real ? __ldg(w) : 0u;
+            qf[ks][nh][1] = real ? __ldg(w + 4) : 0u;
         }
     }
 
@@ -252,12 +255,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
         }
     }
 
-    // Running state for this thread's two head columns h0 = 2c4, h0 + 1.
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    float o[C::DT][4];
+    // Running state for this thread's head columns 8 nh + 2 c4, + 1.
+    float m_run[NH][2], l_run[NH][2];
+    float o[C::DT][NH][4];
 #pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    for (int nh = 0; nh < NH; ++nh) {
+        m_run[nh][0] = m_run[nh][1] = -INFINITY;
+        l_run[nh][0] = l_run[nh][1] = 0.f;
+#pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt) o[dt][nh][0] = o[dt][nh][1] = o[dt][nh][2] = o[dt][nh][3] = 0.f;
+    }
 
     // ldmatrix lane roles: which 8x8 matrix this lane addresses and which row of it.
     const int lm = lane >> 3, lr = lane & 7;
@@ -296,10 +303,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
         }
 
         // ---- S^T = K . Q^T for the tile's m-tiles (rows = tokens)
-        float sc[C::MT][4];
+        float sc[C::MT][NH][4];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
-            sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) sc[mt][nh][0] = sc[mt][nh][1] = sc[mt][nh][2] = sc[mt][nh][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < C::KS; ++ks) {
                 // matrices: 0 = (tok 0-7, chunk 2ks), 1 = (tok 8-15, 2ks), 2 = (tok 0-7, 2ks+1), 3 = (tok 8-15, 2ks+1)
@@ -307,65 +315,79 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
                 const int c = 2 * ks + (lm >> 1);
                 uint32_t a[4];
                 ldsm_x4(a, kb + tile_off<D>(r, c));
-                M::mma(sc[mt], a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) M::mma(sc[mt][nh], a, qf[ks][nh][0], qf[ks][nh][1]);
             }
         }
         // ---- mask, scale to log2 units, tile max per head column
-        float mx[2] = {-INFINITY, -INFINITY};
+        float mx[NH][2];
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
+        for (int nh = 0; nh < NH; ++nh) {
+            mx[nh][0] = mx[nh][1] = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tok = mt * 16 + g8 + (j >> 1) * 8;
-                const float x = tok < nvalid ? sc[mt][j] * p.scale_log2 : -INFINITY;
-                sc[mt][j] = x;
-                mx[j & 1] = fmaxf(mx[j & 1], x);
+            for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tok = mt * 16 + g8 + (j >> 1) * 8;
+                    const float x = tok < nvalid ? sc[mt][nh][j] * p.scale_log2 : -INFINITY;
+                    sc[mt][nh][j] = x;
+                    mx[nh][j & 1] = fmaxf(mx[nh][j & 1], x);
+                }
             }
         }
+        bool rescale = false;
+        float alpha[NH][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 4));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 8));
-            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 16));
-        }
-        float alpha[2];
+        for (int nh = 0; nh < NH; ++nh) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float mn = fmaxf(m_run[h], mx[h]);
-            alpha[h] = (mn == m_run[h]) ? 1.f : ex2_approx(m_run[h] - mn);
-            m_run[h] = mn;
-            l_run[h] *= alpha[h];
+            for (int h = 0; h < 2; ++h) {
+                float m = mx[nh][h];
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                const float mn = fmaxf(m_run[nh][h], m);
+                alpha[nh][h] = (mn == m_run[nh][h]) ? 1.f : ex2_approx(m_run[nh][h] - mn);
+                rescale = rescale || alpha[nh][h] != 1.f;
+                m_run[nh][h] = mn;
+                l_run[nh][h] *= alpha[nh][h];
+            }
         }
-        if (alpha[0] != 1.f || alpha[1] != 1.f) {
+        if (rescale) {
 #pragma unroll
             for (int dt = 0; dt < C::DT; ++dt) {
-                o[dt][0] *= alpha[0];
-                o[dt][1] *= alpha[1];
-                o[dt][2] *= alpha[0];
-                o[dt][3] *= alpha[1];
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) {
+                    o[dt][nh][0] *= alpha[nh][0];
+                    o[dt][nh][1] *= alpha[nh][1];
+                    o[dt][nh][2] *= alpha[nh][0];
+                    o[dt][nh][3] *= alpha[nh][1];
+                }
             }
         }
         // ---- P = exp2(S - m); P^T fragments as hi + lo 16-bit terms
-        uint32_t pb_hi[C::MT][2], pb_lo[C::MT][2];
+        uint32_t pb_hi[C::MT][NH][2], pb_lo[C::MT][NH][2];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
-            float pr[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float x = sc[mt][j];
-                pr[j] = (x == -INFINITY) ? 0.f : ex2_approx(x - m_run[j & 1]);
-                l_run[j & 1] += pr[j];
+            for (int nh = 0; nh < NH; ++nh) {
+                float pr[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x = sc[mt][nh][j];
+                    pr[j] = (x == -INFINITY) ? 0.f : ex2_approx(x - m_run[nh][j & 1]);
+                    l_run[nh][j & 1] += pr[j];
+                }
+                // rows g8 (j = 0, 1) and g8 + 8 (j = 2, 3); columns 2c4, 2c4 + 1
+                const uint32_t h01 = M::pack(pr[0], pr[1]);
+                const uint32_t h23 = M::pack(pr[2], pr[3]);
+                const float2 f01 = unpack2<T>(h01), f23 = unpack2<T>(h23);
+                const uint32_t l01 = M::pack(pr[0] - f01.x, pr[1] - f01.y);
+                const uint32_t l23 = M::pack(pr[2] - f23.x, pr[3] - f23.y);
+                pb_hi[mt][nh][0] = movm_t(h01);
+                pb_hi[mt][nh][1] = movm_t(h23);
+                pb_lo[mt][nh][0] = movm_t(l01);
+                pb_lo[mt][nh][1] = movm_t(l23);
             }
-            // rows g8 (j = 0, 1) and g8 + 8 (j = 2, 3); columns 2c4, 2c4 + 1
-            const uint32_t h01 = M::pack(pr[0], pr[1]);
-            const uint32_t h23 = M::pack(pr[2], pr[3]);
-            const float2 f01 = unpack2<T>(h01), f23 = unpack2<T>(h23);
-            const uint32_t l01 = M::pack(pr[0] - f01.x, pr[1] - f01.y);
-            const uint32_t l23 = M::pack(pr[2] - f23.x, pr[3] - f23.y);
-            pb_hi[mt][0] = movm_t(h01);
-            pb_hi[mt][1] = movm_t(h23);
-            pb_lo[mt][0] = movm_t(l01);
-            pb_lo[mt][1] = movm_t(l23);
         }
         // ---- O^T += V^T . P^T   (k = tokens of each m-tile)
         const bool partial = nvalid < C::TW;
@@ -391,8 +413,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
                     a[2] &= keep89;
                     a[3] &= keep89;
                 }
-                M::mma(o[dt], a, pb_hi[mt][0], pb_hi[mt][1]);
-                M::mma(o[dt], a, pb_lo[mt][0], pb_lo[mt][1]);
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) {
+                    M::mma(o[dt][nh], a, pb_hi[mt][nh][0], pb_hi[mt][nh][1]);
+                    M::mma(o[dt][nh], a, pb_lo[mt][nh][0], pb_lo[mt][nh][1]);
+                }
             }
         }
         if (patched) fence_proxy_async_smem();  // our stores precede the next TMA write of the stage
@@ -432,28 +457,35 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     // (its TMA copies have all landed); after one CTA barrier every thread builds 8
     // output channels of one head.
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
-        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+    for (int nh = 0; nh < NH; ++nh) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            l_run[nh][h] += __shfl_xor_sync(0xffffffffu, l_run[nh][h], 4);
+            l_run[nh][h] += __shfl_xor_sync(0xffffffffu, l_run[nh][h], 8);
+            l_run[nh][h] += __shfl_xor_sync(0xffffffffu, l_run[nh][h], 16);
+        }
     }
     constexpr int OS = C::OS;
+    static_assert((2 * HP + HP * OS) * 4 <= C::ST * C::STAGE_BYTES, "a warp's combine state fits its stages");
     auto state = [&](int w) { return reinterpret_cast<float *>(pipe + w * C::ST * C::STAGE_BYTES); };
     {
-        float *st = state(warp);  // [8] m, [8] l, [8][OS] O
-        if (g8 == 0) {
-            st[2 * c4] = m_run[0];
-            st[2 * c4 + 1] = m_run[1];
-            st[8 + 2 * c4] = l_run[0];
-            st[8 + 2 * c4 + 1] = l_run[1];
-        }
+        float *st = state(warp);  // [HP] m, [HP] l, [HP][OS] O
 #pragma unroll
-        for (int dt = 0; dt < C::DT; ++dt) {
-            float *ow = st + 16 + (2 * c4) * OS + dt * 16 + g8;
-            ow[0] = o[dt][0];
-            ow[OS] = o[dt][1];
-            ow[8] = o[dt][2];
-            ow[OS + 8] = o[dt][3];
+        for (int nh = 0; nh < NH; ++nh) {
+            if (g8 == 0) {
+                st[8 * nh + 2 * c4] = m_run[nh][0];
+                st[8 * nh + 2 * c4 + 1] = m_run[nh][1];
+                st[HP + 8 * nh + 2 * c4] = l_run[nh][0];
+                st[HP + 8 * nh + 2 * c4 + 1] = l_run[nh][1];
+            }
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt) {
+                float *ow = st + 2 * HP + (8 * nh + 2 * c4) * OS + dt * 16 + g8;
+                ow[0] = o[dt][nh][0];
+                ow[OS] = o[dt][nh][1];
+                ow[8] = o[dt][nh][2];
+                ow[OS + 8] = o[dt][nh][3];
+            }
         }
     }
     if (p.defer_wait) {
@@ -470,14 +502,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
         float mw[C::NW], Mx = -INFINITY;
 #pragma unroll
         for (int w = 0; w < C::NW; ++w) {
-            mw[w] = state(w)[h];
+            mw[w] = state(w)[h];  // heads < G <= HP
             Mx = fmaxf(Mx, mw[w]);
         }
         float fw[C::NW], L = 0.f;
 #pragma unroll
         for (int w = 0; w < C::NW; ++w) {
             fw[w] = (mw[w] == -INFINITY) ? 0.f : ex2_approx(mw[w] - Mx);
-            L += state(w)[8 + h] * fw[w];
+            L += state(w)[HP + h] * fw[w];
         }
         // L == 0 only when no key was admissible; a NaN (poisoned row) propagates.
         const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
@@ -486,8 +518,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
         for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
 #pragma unroll
         for (int w = 0; w < C::NW; ++w) {
-            const float4 a = *reinterpret_cast<const float4 *>(state(w) + 16 + h * OS + c8);
-            const float4 b = *reinterpret_cast<const float4 *>(state(w) + 16 + h * OS + c8 + 4);
+            const float4 a = *reinterpret_cast<const float4 *>(state(w) + 2 * HP + h * OS + c8);
+            const float4 b = *reinterpret_cast<const float4 *>(state(w) + 2 * HP + h * OS + c8 + 4);
             const float f = fw[w] * inv;
             acc[0] += a.x * f; acc[1] += a.y * f; acc[2] += a.z * f; acc[3] += a.w * f;
             acc[4] += b.x * f; acc[5] += b.y * f; acc[6] += b.z * f; acc[7] += b.w * f;
@@ -520,21 +552,29 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, STAGES == 2 ? 3 : 2)
     }
 }
 
-template <int D, int STAGES, typename T>
-cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
-                                int num_items, bool pdl, cudaStream_t stream) {
-    using C = TcCfg<D, STAGES>;
-    auto kern = decode_tc_kernel<D, STAGES, T>;
+// Raises the kernel's dynamic shared-memory limit once per device.
+template <int D, int STAGES, int NH, typename T>
+cudaError_t configure_decode_tc() {
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 TcCfg<D, STAGES>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int D, int STAGES, int NH, typename T>
+cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
+                                int num_items, bool pdl, cudaStream_t stream) {
+    using C = TcCfg<D, STAGES>;
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, T>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
     cfg.blockDim = dim3(C::NW * 32);
@@ -545,14 +585,34 @@ cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtens
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p, group);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, T>, tm_k, tm_v, p, group);
+}
+
+// CTAs of one per-item kernel variant resident on an SM at once (registers and
+// shared memory), the slot count of the split heuristic.
+template <int D, int STAGES, int NH, typename T>
+cudaError_t decode_tc_blocks_per_sm_st(int *blocks) {
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, T>();
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_tc_kernel<D, STAGES, NH, T>,
+                                                         TcCfg<D, STAGES>::NW * 32, TcCfg<D, STAGES>::SMEM_BYTES);
+}
+
+template <int D, typename T>
+cudaError_t decode_tc_blocks_per_sm(int stages, int group, int *blocks) {
+    if (group > 8)
+        return stages == 3 ? decode_tc_blocks_per_sm_st<D, 3, 2, T>(blocks) : decode_tc_blocks_per_sm_st<D, 2, 2, T>(blocks);
+    return stages == 3 ? decode_tc_blocks_per_sm_st<D, 3, 1, T>(blocks) : decode_tc_blocks_per_sm_st<D, 2, 1, T>(blocks);
 }
 
 template <int D, typename T>
 cudaError_t launch_decode_tc(int stages, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const DecodeParams &p, int num_items, bool pdl, cudaStream_t stream) {
-    return stages == 3 ? launch_decode_tc_st<D, 3, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
-                       : launch_decode_tc_st<D, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    if (group > 8)
+        return stages == 3 ? launch_decode_tc_st<D, 3, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                           : launch_decode_tc_st<D, 2, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return stages == 3 ? launch_decode_tc_st<D, 3, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                       : launch_decode_tc_st<D, 2, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 }  // namespace pgqa

@@ -213,6 +213,15 @@ def ragged(seed: int = 0, n_decode: int = 127, chunk: int = 512, cached: int = 1
                               f"Hq14/Hkv2/d64, bf16, pool {num_pages}")
 
 
+def wide_group(seed: int = 0, batch: int = 64, cached: int = 2048, num_pages: int = 8400) -> Workload:
+    """A 16-wide query group (32 query heads over 2 kv heads, head_dim 128): the
+    decode tile's two-n-tile form."""
+    return custom(f"wide_group_{batch}x{cached}", [cached + 1] * batch, 16, 32, 2, 128, "bf16",
+                  num_pages, seed=seed, append_last=True,
+                  description=f"{batch} requests x {cached} cached tokens + 1 appended, page 16, "
+                              f"Hq32/Hkv2/d128 (group 16), bf16, pool {num_pages} pages")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen05_decode": qwen05_decode,
@@ -220,6 +229,7 @@ WORKLOADS = {
     "long_context_b1": lambda seed=0: long_context(seed, batch=1),
     "long_context_b4": lambda seed=0: long_context(seed, batch=4),
     "ragged": ragged,
+    "wide_group": wide_group,
 }
 
 

@@ -79,7 +79,8 @@ def _plan(**kw):
     (dict(head_dim=96), "PGQA_ERR_UNSUPPORTED"),
     (dict(page_size=48), "PGQA_ERR_UNSUPPORTED"),
     (dict(num_qo_heads=5), "PGQA_ERR_INVALID_ARG"),
-    (dict(num_qo_heads=18), "PGQA_ERR_UNSUPPORTED"),
+    (dict(num_qo_heads=34), "PGQA_ERR_UNSUPPORTED"),                         # 17 heads per kv head
+    (dict(num_qo_heads=18, decode_kernel="cuda_core"), "PGQA_ERR_UNSUPPORTED"),  # 9: CUDA-core limit is 8
     (dict(dtype=torch.float32), "PGQA_ERR_UNSUPPORTED"),
     (dict(max_batch=0), "PGQA_ERR_INVALID_ARG"),
 ])

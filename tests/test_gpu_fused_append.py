@@ -68,13 +68,16 @@ def test_fused_decode_step(opts, pool_stable):
     check_pool(w, dev)
 
 
-@pytest.mark.parametrize("head_dim,page_size,dtype", [(128, 256, "fp16"), (64, 64, "bf16"), (128, 16, "bf16")])
-def test_fused_shapes(head_dim, page_size, dtype):
-    w = W.custom("fz", [1, 2, 17, 33, 200, 700], page_size, 12, 2, head_dim, dtype, 64, seed=head_dim + page_size)
+@pytest.mark.parametrize("head_dim,page_size,dtype,heads", [(128, 256, "fp16", 12), (64, 64, "bf16", 12),
+                                                             (128, 16, "bf16", 12), (64, 16, "bf16", 32),
+                                                             (128, 32, "fp16", 22)])
+def test_fused_shapes(head_dim, page_size, dtype, heads):
+    w = W.custom("fz", [1, 2, 17, 33, 200, 700], page_size, heads, 2, head_dim, dtype, 64,
+                 seed=head_dim + page_size + heads)
     new_rows_for_query_rows(w)
     ro, rl = H.oracle_outputs(w)
     out, lse, dev, _ = fused_gpu(w, split_tokens=64)
-    H.compare(out, lse, ro, rl, f"fused d{head_dim} ps{page_size} {dtype}")
+    H.compare(out, lse, ro, rl, f"fused d{head_dim} ps{page_size} {dtype} Hq{heads}")
     check_pool(w, dev)
 
 

@@ -54,6 +54,28 @@ def test_groups(group, dtype, head_dim, kernel):
     H.compare(out, lse, ro, rl, f"{kernel}/g{group}/{dtype}/d{head_dim}")
 
 
+@pytest.mark.parametrize("group,dtype,head_dim",
+                         [(g, dt, d) for g in range(9, 17) for dt, d in (("bf16", 64), ("fp16", 128))] +
+                         [(16, "fp16", 64), (12, "bf16", 128)])
+@pytest.mark.parametrize("stages", [2, 3])
+def test_wide_groups(group, dtype, head_dim, stages):
+    """9..16 query heads per kv head: the tensor-core tile's second 8-head n tile."""
+    w = W.custom("wgrp", [3, 40, 129, 300, 1000], 16, group * 2, 2, head_dim, dtype, 128,
+                 seed=group * 5 + head_dim + stages)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64, pipeline_stages=stages)
+    H.compare(out, lse, ro, rl, f"wide g{group}/{dtype}/d{head_dim}/st{stages}")
+
+
+@pytest.mark.parametrize("decode_ctas", [-1, 3])
+def test_wide_group_persistent_request_runs_per_item(decode_ctas):
+    """A persistent schedule asked for with a 16-head group runs one CTA per item."""
+    w = W.custom("wgp", [17, 300, 64], 32, 16, 1, 128, "bf16", 32, seed=3)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, _ = H.gpu_outputs(w, split_tokens=64, decode_ctas=decode_ctas)
+    H.compare(out, lse, ro, rl, f"wide persistent {decode_ctas}")
+
+
 def test_all_empty_batch():
     w = W.custom("empty", [0, 0, 0], 16, 4, 2, 64, "bf16", 4, seed=1)
     out, lse, _ = H.gpu_outputs(w)
@@ -89,7 +111,8 @@ def test_explicit_scale():
 
 @pytest.mark.parametrize("group,head_dim,page_size,dtype",
                          [(7, 64, 64, "bf16"), (6, 128, 256, "fp16"), (1, 64, 16, "bf16"), (8, 128, 32, "bf16"),
-                          (3, 64, 128, "fp16"), (5, 128, 16, "bf16")])
+                          (3, 64, 128, "fp16"), (5, 128, 16, "bf16"), (16, 64, 64, "bf16"),
+                          (12, 128, 16, "fp16")])
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_segments(group, head_dim, page_size, dtype, causal):
     """Chunks of query rows (tensor-core prefill tiles) mixed with decode rows,
