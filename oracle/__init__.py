@@ -76,6 +76,14 @@ class Oracle:
             ctypes.c_int, _i32p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int64,
             ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_double,
             _f64p, _f64p]
+        lib.oracle_narrow.restype = ctypes.c_uint16
+        lib.oracle_narrow.argtypes = [ctypes.c_double, ctypes.c_int]
+        lib.oracle_rope_f64.restype = ctypes.c_int
+        lib.oracle_rope_f64.argtypes = [_f64p, _f64p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i32p,
+                                        ctypes.c_double]
+        lib.oracle_rope.restype = ctypes.c_int
+        lib.oracle_rope.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_double,
+                                    ctypes.c_int, _f64p, _u16p]
         self.lib = lib
 
     # -- scalar helpers ---------------------------------------------------
@@ -83,6 +91,43 @@ class Oracle:
         code = DTYPE_CODES[dtype]
         flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
         return np.array([self.lib.oracle_widen(int(b), code) for b in flat]).reshape(np.shape(bits))
+
+    def narrow(self, values: np.ndarray, dtype: str) -> np.ndarray:
+        """fp64 values -> 16-bit patterns, rounded once to nearest, ties to even."""
+        code = DTYPE_CODES[dtype]
+        flat = np.ascontiguousarray(values, dtype=np.float64).ravel()
+        return np.array([self.lib.oracle_narrow(float(v), code) for v in flat],
+                        dtype=np.uint16).reshape(np.shape(values))
+
+    # -- rotary position embedding ----------------------------------------
+    def rope_f64(self, x: np.ndarray, positions, theta: float) -> np.ndarray:
+        """x [rows, heads, d] fp64 -> rotated fp64 (positions [rows])."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        positions = np.ascontiguousarray(positions, dtype=np.int32)
+        rows, heads, d = x.shape
+        assert positions.shape == (rows,)
+        y = np.empty_like(x)
+        rc = self.lib.oracle_rope_f64(_ptr(x, _f64p), _ptr(y, _f64p), rows, heads, d,
+                                      _ptr(positions, _i32p), float(theta))
+        if rc != 0:
+            raise ValueError(f"oracle_rope_f64 failed (code {rc})")
+        return y
+
+    def rope(self, x: np.ndarray, positions, theta: float, dtype: str):
+        """x [rows, heads, d] uint16 -> (rotated uint16, rotated fp64 before rounding)."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        positions = np.ascontiguousarray(positions, dtype=np.int32)
+        rows, heads, d = x.shape
+        assert positions.shape == (rows,)
+        out64 = np.empty(x.shape, np.float64)
+        out16 = np.empty(x.shape, np.uint16)
+        if rows == 0:
+            return out16, out64
+        rc = self.lib.oracle_rope(_ptr(x, _u16p), rows, heads, d, _ptr(positions, _i32p), float(theta),
+                                  DTYPE_CODES[dtype], _ptr(out64, _f64p), _ptr(out16, _u16p))
+        if rc != 0:
+            raise ValueError(f"oracle_rope failed (code {rc})")
+        return out16, out64
 
     def check_page_table(self, kv_indptr, kv_indices, last_page_len, num_pages, page_size) -> int:
         kv_indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)

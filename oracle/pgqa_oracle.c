@@ -34,7 +34,13 @@
  *     N keys may attend keys j <= N - L + i;
  *   - scale defaults to 1/sqrt(head_dim); lse is the natural log-sum-exp of the
  *     scaled scores; a row with no admissible key has o = 0 and lse = -inf;
- *   - a negative slot in the append means "skip this token".
+ *   - a negative slot in the append means "skip this token";
+ *   - RoPE, which the pages name but do not write out ("flashlet" README,
+ *     milestones: a RoPE fusion kernel; "Torchlet", introduction: the
+ *     Qwen2.5-style model includes RoPE), is read as the rotate-half form of the
+ *     Qwen2.5 models: channel i < d/2 pairs with channel i + d/2 and both turn
+ *     by the angle pos * theta^(-2i/d), theta a parameter; the rotated value is
+ *     rounded once to the 16-bit type, to nearest with ties to even.
  *
  * Everything is fp64.  16-bit inputs are widened exactly (every bf16 and fp16
  * value is a double).
@@ -384,5 +390,116 @@ int oracle_attention_partial(const uint16_t *q, const uint16_t *k_pool, const ui
         qv[c] = oracle_widen(q[(r * Hq + h) * (int64_t)d + c], dtype);
     int rc = attend_range(qv, K, V, j0, j1, d, scale, o, lse);
     free(K); free(V); free(qv);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Narrowing and the rotary position embedding.                             */
+/* ------------------------------------------------------------------------ */
+
+/* Rounds x to the 16-bit type, to nearest with ties to even, straight from the
+ * double (no binary32 step in between, which could round twice) and returns
+ * the bit pattern.  bf16: 8 significant bits, exponents -126..127 (the range of
+ * binary32); fp16: 11 significant bits, exponents -14..15.  Below the smallest
+ * normal the spacing stays that of the smallest binade (subnormals); past the
+ * largest finite value the result is infinity; NaN stays NaN. */
+uint16_t oracle_narrow(double x, int dtype)
+{
+    const int bf = dtype == ORACLE_BF16;
+    const int prec = bf ? 8 : 11;
+    const int emin = bf ? -126 : -14, emax = bf ? 127 : 15;
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x))
+        return (uint16_t)(sign | (bf ? 0x7FC0u : 0x7E00u));
+    const uint16_t inf = (uint16_t)(sign | (bf ? 0x7F80u : 0x7C00u));
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return inf;
+    int ex;
+    frexp(a, &ex);            /* a = f * 2^ex, f in [0.5, 1): binade exponent ex - 1 */
+    int e = ex - 1;
+    if (e < emin)
+        e = emin;
+    /* a in units of the spacing 2^(e - prec + 1): an integer part and an exact fraction */
+    double y = ldexp(a, prec - 1 - e);
+    double fl = floor(y), frac = y - fl;
+    double r = fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0))
+        r = fl + 1.0;
+    /* r * 2^(e - prec + 1); r may have carried to 2^prec (the next binade) */
+    int eb = e;
+    if (r >= ldexp(1.0, prec)) {
+        r = ldexp(r, -1);
+        eb = e + 1;
+    }
+    if (eb > emax)
+        return inf;
+    uint32_t mant = (uint32_t)r;  /* prec bits when normal, fewer when subnormal */
+    int normal = mant >= (1u << (prec - 1));
+    uint32_t bits;
+    if (bf) {
+        int biased = normal ? eb + 127 : 0;
+        bits = ((uint32_t)biased << 7) | (mant & 0x7Fu);
+    } else {
+        int biased = normal ? eb + 15 : 0;
+        bits = ((uint32_t)biased << 10) | (mant & 0x3FFu);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+/* Rotary position embedding in fp64 on rows [rows, heads, d] at positions[rows]:
+ * for i < d/2, with phi = positions[r] * theta^(-2i/d),
+ *     y[i]       = x[i] cos(phi) - x[i + d/2] sin(phi)
+ *     y[i + d/2] = x[i + d/2] cos(phi) + x[i] sin(phi). */
+int oracle_rope_f64(const double *x, double *y, int64_t rows, int heads, int d,
+                    const int32_t *positions, double theta)
+{
+    if (rows < 0 || heads <= 0 || d <= 0 || d % 2 != 0 || !(theta > 0.0))
+        return ORACLE_ERR_ARG;
+    const int half = d / 2;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double pos = (double)positions[r];
+        for (int i = 0; i < half; ++i) {
+            const double phi = pos * pow(theta, -2.0 * i / d);
+            const double c = cos(phi), s = sin(phi);
+            for (int h = 0; h < heads; ++h) {
+                const int64_t base = (r * heads + h) * (int64_t)d;
+                const double a = x[base + i], b = x[base + i + half];
+                y[base + i] = a * c - b * s;
+                y[base + i + half] = b * c + a * s;
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The same on 16-bit patterns: widened exactly, rotated in fp64, then (out16)
+ * narrowed once; out64 (optional) receives the fp64 values before rounding. */
+int oracle_rope(const uint16_t *x, int64_t rows, int heads, int d, const int32_t *positions,
+                double theta, int dtype, double *out64, uint16_t *out16)
+{
+    if (rows < 0 || heads <= 0 || d <= 0)
+        return ORACLE_ERR_ARG;
+    const int64_t n = rows * heads * (int64_t)d;
+    if (n == 0)
+        return ORACLE_OK;
+    double *xin = (double *)malloc((size_t)n * sizeof(double));
+    double *y = (double *)malloc((size_t)n * sizeof(double));
+    if (!xin || !y) {
+        free(xin); free(y);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t k = 0; k < n; ++k)
+        xin[k] = oracle_widen(x[k], dtype);
+    int rc = oracle_rope_f64(xin, y, rows, heads, d, positions, theta);
+    if (rc == ORACLE_OK) {
+        for (int64_t k = 0; k < n; ++k) {
+            if (out64) out64[k] = y[k];
+            if (out16) out16[k] = oracle_narrow(y[k], dtype);
+        }
+    }
+    free(xin); free(y);
     return rc;
 }

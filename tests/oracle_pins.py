@@ -368,4 +368,153 @@ def pin_empty_request(orc):
     assert np.isfinite(lse[1]).all()
 
 
+# ---------------------------------------------------------------------------
+# rounding to the 16-bit types (used by the rotary embedding)
+# ---------------------------------------------------------------------------
+
+def _grid(dtype):
+    """Every finite non-negative 16-bit value (decoded by torch / numpy) with its pattern, ascending."""
+    bits = np.arange(0x8000, dtype=np.uint16)  # sign bit clear
+    if dtype == "bf16":
+        vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    else:
+        vals = bits.view(np.float16).astype(np.float64)
+    keep = np.isfinite(vals)
+    return vals[keep], bits[keep]
+
+
+def nearest_even(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Brute-force round to nearest, ties to the even pattern, over the whole grid of
+    finite values; |x| at or past the largest value plus half its spacing is infinity."""
+    vals, bits = _grid(dtype)
+    top, gap = vals[-1], vals[-1] - vals[-2]
+    inf = np.uint16(0x7F80 if dtype == "bf16" else 0x7C00)
+    out = np.empty(x.shape, np.uint16)
+    for k, xv in enumerate(np.asarray(x, np.float64).ravel()):
+        a = abs(xv)
+        sign = np.uint16(0x8000) if np.signbit(xv) else np.uint16(0)
+        if a >= top + gap / 2:
+            out.flat[k] = sign | inf
+            continue
+        j = int(np.searchsorted(vals, a))
+        cands = [c for c in (j - 1, j) if 0 <= c < len(vals)]
+        dist = [abs(vals[c] - a) for c in cands]
+        best = [c for c, dd in zip(cands, dist) if dd == min(dist)]
+        pick = best[0] if len(best) == 1 else next(c for c in best if bits[c] % 2 == 0)
+        out.flat[k] = sign | bits[pick]
+    return out
+
+
+def _narrow_cases(dtype, seed):
+    """Random magnitudes over the whole range (subnormals and overflow included), exact
+    ties between neighbours, and values just past a tie that binary32 would round onto
+    the tie (a two-step rounding through binary32 lands on the wrong side)."""
+    rng = np.random.default_rng(seed)
+    vals, _ = _grid(dtype)
+    lo, hi = (-136, 129) if dtype == "bf16" else (-26, 17)
+    rand = np.ldexp(1.0 + rng.random(400), rng.integers(lo, hi, 400)) * rng.choice([-1.0, 1.0], 400)
+    k = rng.integers(0, len(vals) - 1, 300)
+    ties = (vals[k] + vals[k + 1]) / 2
+    k2 = rng.integers(1, len(vals) - 1, 300)
+    mids = (vals[k2] + vals[k2 + 1]) / 2
+    traps = np.concatenate([mids * (1 + 2.0 ** -33), mids * (1 - 2.0 ** -33)])
+    top, gap = vals[-1], vals[-1] - vals[-2]
+    edges = np.array([0.0, -0.0, top, top + gap / 2, top + gap / 2 * (1 - 2.0 ** -40), vals[1] / 2,
+                      vals[1] / 2 * (1 + 2.0 ** -30), vals[1] * 0.75, 1.0, -1.0, np.inf, -np.inf])
+    return np.concatenate([rand, ties, -ties, traps, edges])
+
+
+def pin_narrow_bf16(orc):
+    x = _narrow_cases("bf16", 1)
+    assert np.array_equal(orc.narrow(x, "bf16"), nearest_even(x, "bf16")), "bf16 rounding"
+
+
+def pin_narrow_fp16(orc):
+    x = _narrow_cases("fp16", 2)
+    got = orc.narrow(x, "fp16")
+    assert np.array_equal(got, nearest_even(x, "fp16")), "fp16 rounding (brute force)"
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, ref), "fp16 rounding (numpy)"
+
+
+# ---------------------------------------------------------------------------
+# rotary position embedding
+# ---------------------------------------------------------------------------
+
+def _rand16(shape, dtype, seed):
+    gen = torch.Generator().manual_seed(seed)
+    t = torch.randn(*shape, generator=gen).to(W.TORCH_DTYPES[dtype])
+    return W.raw16(t).reshape(shape)
+
+
+def pin_rope_position_zero(orc):
+    """At position 0 every angle is 0: the rotation is the identity, bit for bit."""
+    for dt in ("bf16", "fp16"):
+        x = _rand16((5, 3, 64), dt, 4)
+        out16, _ = orc.rope(x, np.zeros(5, np.int32), 1.0e6, dt)
+        assert np.array_equal(out16, x), dt
+
+
+def pin_rope_unit_vectors(orc):
+    """Unit vector e_i (i < d/2) at position p turns into cos(phi) e_i + sin(phi) e_(i+d/2),
+    and e_(i+d/2) into cos(phi) e_(i+d/2) - sin(phi) e_i, phi = p * theta^(-2i/d): which
+    channels pair, which way they turn and how fast each pair turns."""
+    d, theta = 16, 1.0e4
+    pos = np.array([1, 7, 300, 40001], np.int32)
+    for i in range(d // 2):
+        for second in (False, True):
+            x = np.zeros((len(pos), 1, d))
+            x[:, 0, i + (d // 2 if second else 0)] = 1.0
+            y = orc.rope_f64(x, pos, theta)
+            phi = pos.astype(np.float64) * np.power(theta, -2.0 * i / d)
+            ref = np.zeros_like(x)
+            if second:
+                ref[:, 0, i], ref[:, 0, i + d // 2] = -np.sin(phi), np.cos(phi)
+            else:
+                ref[:, 0, i], ref[:, 0, i + d // 2] = np.cos(phi), np.sin(phi)
+            _close(y, ref, 1e-9, f"unit vector {i} second={second}")
+
+
+def pin_rope_relative_position(orc):
+    """The defining property: q.k after rotating q to m and k to n depends on m - n only."""
+    rng = np.random.default_rng(5)
+    q, k = rng.standard_normal((1, 4, 64)), rng.standard_normal((1, 4, 64))
+    def dot(m, n):
+        return np.sum(orc.rope_f64(q, np.array([m], np.int32), 1.0e6) *
+                      orc.rope_f64(k, np.array([n], np.int32), 1.0e6), axis=-1)
+    base = dot(40, 13)
+    for t in (1, 977, 30000):
+        _close(dot(40 + t, 13 + t), base, 1e-9, f"shift {t}")
+    _close(dot(77, 77), np.sum(q * k, axis=-1), 1e-9, "equal positions")
+
+
+def pin_rope_composition(orc):
+    """Rotating to p1 and then by p2 equals rotating to p1 + p2."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((3, 2, 32))
+    p1, p2 = np.array([5, 1000, 31], np.int32), np.array([2, 65, 12345], np.int32)
+    two = orc.rope_f64(orc.rope_f64(x, p1, 1.0e6), p2, 1.0e6)
+    _close(two, orc.rope_f64(x, p1 + p2, 1.0e6), 1e-9, "composition")
+
+
+def pin_rope_pair_norms(orc):
+    """Each (i, i + d/2) pair keeps its length."""
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((6, 3, 128))
+    y = orc.rope_f64(x, np.array([0, 1, 9, 500, 8191, 32767], np.int32), 1.0e6)
+    h = 64
+    _close(np.hypot(y[..., :h], y[..., h:]), np.hypot(x[..., :h], x[..., h:]), 1e-12, "pair norms")
+
+
+def pin_rope_rounding(orc):
+    """The 16-bit result is the fp64 rotation rounded once, to nearest even."""
+    for dt in ("bf16", "fp16"):
+        x = _rand16((4, 2, 64), dt, 8)
+        out16, out64 = orc.rope(x, np.array([3, 100, 4096, 30001], np.int32), 1.0e6, dt)
+        assert np.array_equal(out16, nearest_even(out64, dt)), dt
+        _close(out64, orc.rope_f64(orc.widen(x, dt), np.array([3, 100, 4096, 30001], np.int32), 1.0e6),
+               0.0, f"{dt} widen-then-rotate")
+
+
 PINS = {name: fn for name, fn in globals().items() if name.startswith("pin_")}

@@ -40,6 +40,16 @@ MUTANTS = {
     "softmax_sign": ("w[j - j0] = exp(w[j - j0] - m);", "w[j - j0] = exp(m - w[j - j0]);"),
     "query_head_index": ("qv[c] = oracle_widen(p->q[(r * p->Hq + h) * (int64_t)d + c], p->dtype);",
                          "qv[c] = oracle_widen(p->q[(r * p->Hq + (h / g) * g) * (int64_t)d + c], p->dtype);"),
+    "narrow_via_binary32": ("double a = fabs(x);\n    if (a == 0.0)", "double a = fabs((double)(float)x);\n    if (a == 0.0)"),
+    "narrow_ties_away": ("(frac == 0.5 && fmod(fl, 2.0) != 0.0)", "(frac == 0.5)"),
+    "narrow_no_subnormal_floor": ("if (e < emin)\n        e = emin;", "if (e < emin - 64)\n        e = emin;"),
+    "narrow_truncates": ("if (frac > 0.5 || (frac", "if (frac > 1.5 || (frac"),
+    "rope_turns_backwards": ("const double c = cos(phi), s = sin(phi);", "const double c = cos(phi), s = -sin(phi);"),
+    "rope_freq_exponent": ("pow(theta, -2.0 * i / d)", "pow(theta, -1.0 * i / d)"),
+    "rope_adjacent_pairs": ("const double a = x[base + i], b = x[base + i + half];",
+                            "const double a = x[base + i], b = x[base + (i + half + 1) % d];"),
+    "rope_second_sign": ("y[base + i + half] = b * c + a * s;", "y[base + i + half] = b * c - a * s;"),
+    "rope_first_position": ("const double pos = (double)positions[r];", "const double pos = (double)positions[0];"),
 }
 
 
