@@ -255,6 +255,7 @@ def step_bytes(w, layers: int) -> dict:
 
 def run_ours(args, rank, world, local):
     import paged_kv_gqa_05_gb300 as pg
+    from paged_kv_gqa_05_gb300 import workloads as W
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
@@ -265,8 +266,11 @@ def run_ours(args, rank, world, local):
     plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dt, max_batch=w.batch,
                    max_q_rows=w.rows, max_splits=args.max_splits, split_tokens=args.split_tokens,
                    ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel,
-                   pipeline_stages=args.stages, decode_ctas=args.decode_ctas)
+                   pipeline_stages=args.stages, decode_ctas=args.decode_ctas,
+                   rope_theta=args.rope_theta, rope_max_position=int(w.kv_lens.max()) if args.rope_theta > 0 else 0)
     stream = torch.cuda.Stream(device)
+    positions = (torch.from_numpy(W.row_positions(w)).to(device)
+                 if args.rope_theta > 0 and L["slots"] is not None else None)
     launches_per_layer = {}
 
     def update_plan():
@@ -283,7 +287,10 @@ def run_ours(args, rank, world, local):
                 pg.append_run(plan.handle, L["k_new"][l], L["v_new"][l], L["q"][l], L["k_pool"][l],
                               L["v_pool"][l], out=L["out"][l], pool_stable=True, stream=stream)
                 continue
-            if with_append and L["slots"] is not None:
+            if with_append and L["slots"] is not None and positions is not None:
+                plan.kv_append_rope(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
+                                    positions, stream=stream)
+            elif with_append and L["slots"] is not None:
                 pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
                              stream=stream)
             pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l], stream=stream)
@@ -400,6 +407,7 @@ def run_ours(args, rank, world, local):
             "l2": f"inputs larger than L2: {layers} independent layer pools per step",
             "graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single",
             "decode_kernel": args.decode_kernel, "append_mode": args.append_mode if L["slots"] is not None else None,
+            "rope_theta": args.rope_theta if args.rope_theta > 0 else None,
             "plan": {k: info[k] for k in ("num_items", "num_merge_tasks", "split_tokens", "max_splits_used",
                                           "num_sms")},
         },
@@ -533,6 +541,8 @@ def main(argv=None):
                     help="0: one CTA per work item; n: n persistent CTAs; -1: one persistent CTA per SM")
     ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
+    ap.add_argument("--rope-theta", type=float, default=0.0,
+                    help="> 0: rotary embedding of q and the appended K rows with this base")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

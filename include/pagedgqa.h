@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define PGQA_ABI_VERSION 1
+#define PGQA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define PGQA_API __attribute__((visibility("default")))
@@ -66,6 +66,7 @@ typedef enum pgqa_dtype { PGQA_BF16 = 0, PGQA_FP16 = 1, PGQA_FP32 = 2 } pgqa_dty
 #define PGQA_FLAG_SLOT_RANGE 2u   /* an append slot >= num_pages * page_size was skipped */
 #define PGQA_FLAG_WAIT_TIMEOUT 4u /* a pipeline barrier wait gave up (bounded spin) */
 #define PGQA_FLAG_SMEM_ALIGN 8u   /* shared memory too coarsely aligned for the TMA layout; CTA skipped */
+#define PGQA_FLAG_ROPE_POSITION 16u /* a rotary position outside [0, rope_max_position) was skipped */
 
 PGQA_API int pgqa_abi_version(void);
 PGQA_API const char *pgqa_status_string(pgqa_status status);
@@ -133,7 +134,34 @@ typedef struct pgqa_plan_config {
                              n > 0 = n persistent CTAs walking the work list; -1 = one
                              persistent CTA per SM.  Groups wider than 8 heads always run
                              one CTA per item. */
+    int rope_max_position; /* RoPE plans: positions 0 .. rope_max_position - 1 are valid */
+    double rope_theta;    /* > 0: rotary position embedding with this base (see below);
+                             0: none */
 } pgqa_plan_config;
+
+/*
+ * Rotary position embedding (RoPE).  The "flashlet" README lists a RoPE fusion
+ * kernel among its milestones and "Torchlet"'s Qwen2.5-style model includes
+ * RoPE; neither writes it out.  It is taken in the rotate-half form of the
+ * Qwen2.5 models: for i < head_dim/2, channels i and i + head_dim/2 turn by
+ * phi = pos * rope_theta^(-2i/head_dim):
+ *     x'[i]            = x[i] cos(phi) - x[i + head_dim/2] sin(phi)
+ *     x'[i + head_dim/2] = x[i + head_dim/2] cos(phi) + x[i] sin(phi).
+ * A plan with rope_theta > 0 builds a (cos, sin) table of rope_max_position
+ * rows (fp64 angles rounded to fp32; head_dim * 4 bytes per row) once in
+ * pgqa_plan_create, and then:
+ *   - pgqa_run and pgqa_append_run take q BEFORE rotation: each query row is
+ *     rotated at its position, the key position of its own token (a request
+ *     with N keys and L query rows has them at N - L .. N - 1);
+ *   - pgqa_append_run takes k_new before rotation and stores (and attends) it
+ *     rotated at its key position; v_new is not rotated;
+ *   - the pool holds rotated keys (pgqa_kv_append_rope writes them).
+ * The rotation runs in fp32 and rounds once to the plan's dtype (nearest, ties
+ * to even).  plan_update rejects a request whose query rows outnumber its keys
+ * or whose keys reach past rope_max_position (PGQA_ERR_INVALID_ARG).  RoPE
+ * plans need the tensor-core kernels (PGQA_ERR_UNSUPPORTED with
+ * PGQA_DECODE_CUDA_CORE) and run one CTA per work item.
+ */
 
 #define PGQA_DECODE_AUTO 0
 #define PGQA_DECODE_TENSOR_CORE 1
@@ -141,10 +169,33 @@ typedef struct pgqa_plan_config {
 
 /*
  * Creates a plan on the current device.  Allocates its device and pinned host
- * buffers (the only allocations the library makes).  *plan is set to NULL on
- * failure.
+ * buffers (the only allocations the library makes) and, for a RoPE plan, builds
+ * its rotary table (synchronously).  *plan is set to NULL on failure.
  */
 PGQA_API pgqa_status pgqa_plan_create(pgqa_plan **plan, const pgqa_plan_config *cfg);
+
+/*
+ * pgqa_kv_append_rope -- paged KV append with the plan's rotary embedding on K.
+ *
+ * The append of pgqa_kv_append (the "flashlet" README, design bullets: one copy
+ * of each new token's row into its flat slot) with each K row rotated at
+ * positions[t] on the way (the RoPE fusion of the "flashlet" README's
+ * milestones; the rotation is the one described above).  Shapes, dtype,
+ * head_dim and num_kv_heads are the plan's.
+ *
+ *   k_pool, v_pool  pools [num_pages, page_size, num_kv_heads, head_dim]
+ *   k, v            new rows [num_tokens, num_kv_heads, head_dim], k before rotation
+ *   slot_mapping    [num_tokens] int64, device: as in pgqa_kv_append
+ *   positions       [num_tokens] int32, device: the token's position; a
+ *                   position outside [0, rope_max_position) skips the row (K
+ *                   and V) and raises PGQA_FLAG_ROPE_POSITION
+ * Enqueued on `stream`; ordered after the stream's previous kernel.
+ * Errors: PGQA_ERR_INVALID_ARG for a plan without RoPE, NULL or misaligned
+ * pointers, negative sizes.
+ */
+PGQA_API pgqa_status pgqa_kv_append_rope(const pgqa_plan *plan, void *k_pool, void *v_pool, int64_t num_pages,
+                                         const void *k, const void *v, const int64_t *slot_mapping,
+                                         const int32_t *positions, int64_t num_tokens, pgqa_stream_t stream);
 
 /*
  * pgqa_plan_update -- plan().

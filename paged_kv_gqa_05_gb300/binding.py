@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "PGQA_OK", 1: "PGQA_ERR_INVALID_ARG", 2: "PGQA_ERR_UNSUPPORTE
 # Every entry point include/pagedgqa.h declares.
 EXPORTS = ("pgqa_abi_version", "pgqa_status_string", "pgqa_last_error", "pgqa_read_device_flags",
            "pgqa_kv_append", "pgqa_plan_create", "pgqa_plan_update", "pgqa_run",
-           "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run", "pgqa_decode_static_scratch")
+           "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run", "pgqa_decode_static_scratch",
+           "pgqa_kv_append_rope")
 
 
 class PagedGQAError(RuntimeError):
@@ -46,7 +47,8 @@ class PlanConfig(ctypes.Structure):
                 ("max_splits", ctypes.c_int), ("split_tokens", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("decode_kernel", ctypes.c_int),
                 ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
-                ("decode_ctas", ctypes.c_int)]
+                ("decode_ctas", ctypes.c_int), ("rope_max_position", ctypes.c_int),
+                ("rope_theta", ctypes.c_double)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -95,11 +97,13 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                                ctypes.c_float, _vp]
+    lib.pgqa_kv_append_rope.restype = ctypes.c_int
+    lib.pgqa_kv_append_rope.argtypes = [_vp, _vp, _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp]
     lib.pgqa_plan_destroy.restype = ctypes.c_int
     lib.pgqa_plan_destroy.argtypes = [_vp]
     lib.pgqa_plan_get_info.restype = ctypes.c_int
     lib.pgqa_plan_get_info.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
-    if lib.pgqa_abi_version() != 1:
+    if lib.pgqa_abi_version() != 2:
         raise RuntimeError("libpagedgqa.so ABI version mismatch")
     _lib = lib
     return lib
@@ -160,16 +164,35 @@ def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: to
                               _dev(slot_mapping, "slot_mapping"), k.shape[0], _stream(stream)))
 
 
+def kv_append_rope(plan: int, k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                   slot_mapping: torch.Tensor, positions: torch.Tensor, stream=None) -> None:
+    """pgqa_kv_append_rope: k[t] rotated at positions[t] and v[t] -> flat slot slot_mapping[t]."""
+    P, ps, Hkv, D = k_pool.shape
+    if v_pool.shape != k_pool.shape or k.shape != v.shape or k.shape[1:] != (Hkv, D):
+        raise ValueError("shape mismatch between pools and rows")
+    if k_pool.dtype != k.dtype or v_pool.dtype != k.dtype or v.dtype != k.dtype:
+        raise ValueError("pools and rows must share one dtype")
+    if slot_mapping.dtype != torch.int64 or positions.dtype != torch.int32:
+        raise ValueError("slot_mapping must be int64 and positions int32")
+    if slot_mapping.shape != (k.shape[0],) or positions.shape != (k.shape[0],):
+        raise ValueError("one slot and one position per row")
+    _check(load().pgqa_kv_append_rope(plan, _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), P, _dev(k, "k"),
+                                      _dev(v, "v"), _dev(slot_mapping, "slot_mapping"),
+                                      _dev(positions, "positions"), k.shape[0], _stream(stream)))
+
+
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
-                pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0) -> int:
+                pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0,
+                rope_theta: float = 0.0, rope_max_position: int = 0) -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
-    decode_kernel: "auto" | "tensor_core" | "cuda_core"."""
+    decode_kernel: "auto" | "tensor_core" | "cuda_core"; rope_theta > 0 turns on the
+    rotary embedding of q and the appended K rows (positions < rope_max_position)."""
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
     cfg = PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                      max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
-                     pipeline_stages, prefill_splits, decode_ctas)
+                     pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta))
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value
@@ -265,6 +288,10 @@ def plan_get_info(plan: int) -> dict:
     return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
 
 
+# Bits of the device flag word (include/pagedgqa.h).
+FLAG_PAGE_INDEX, FLAG_SLOT_RANGE, FLAG_WAIT_TIMEOUT, FLAG_SMEM_ALIGN, FLAG_ROPE_POSITION = 1, 2, 4, 8, 16
+
+
 def read_device_flags(clear: bool = True) -> int:
     """Flag word of the current device (synchronises).  0 when no check fired."""
     v = ctypes.c_uint32(0)
@@ -292,6 +319,9 @@ class Plan:
 
     def append_run(self, *args, **kwargs) -> torch.Tensor:
         return append_run(self.handle, *args, **kwargs)
+
+    def kv_append_rope(self, *args, **kwargs) -> None:
+        kv_append_rope(self.handle, *args, **kwargs)
 
     def info(self) -> dict:
         return plan_get_info(self.handle)

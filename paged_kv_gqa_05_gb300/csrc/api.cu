@@ -177,6 +177,7 @@ struct pgqa_plan {
     int max_tasks = 0;
     int max_prefill = 0;     // capacity of the prefill-tile list
     int max_slots = 0;       // capacity of the split partials (slots of G x head_dim floats)
+    float2 *rope_cs = nullptr;  // rotary (cos, sin) table [rope_max_position][head_dim / 2], or null
 
     void *d_meta = nullptr;  // [max_items] WorkItem, [max_tasks] MergeTask, [max_prefill] PrefillItem
     float *d_partial_o = nullptr;
@@ -241,6 +242,7 @@ static void plan_free(pgqa_plan *p) {
     if (p->d_meta) cudaFree(p->d_meta);
     if (p->d_partial_o) cudaFree(p->d_partial_o);
     if (p->d_partial_lse) cudaFree(p->d_partial_lse);
+    if (p->rope_cs) cudaFree(p->rope_cs);
     delete p;
 }
 
@@ -314,6 +316,32 @@ pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_pages, int pa
     return PGQA_OK;
 }
 
+pgqa_status pgqa_kv_append_rope(const pgqa_plan *plan, void *k_pool, void *v_pool, int64_t num_pages, const void *k,
+                                const void *v, const int64_t *slot_mapping, const int32_t *positions,
+                                int64_t num_tokens, pgqa_stream_t stream) {
+    if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
+    if (!plan->rope_cs) return fail(PGQA_ERR_INVALID_ARG, "the plan was created without RoPE (rope_theta 0)");
+    if (num_tokens < 0 || num_pages < 0) return fail(PGQA_ERR_INVALID_ARG, "negative size");
+    if (num_tokens == 0) return PGQA_OK;
+    if (!k_pool || !v_pool || !k || !v || !slot_mapping || !positions)
+        return fail(PGQA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k) || !aligned16(v))
+        return fail(PGQA_ERR_INVALID_ARG, "pool and row pointers must be 16-byte aligned");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != plan->device) return fail(PGQA_ERR_INVALID_ARG, "plan belongs to device %d, current is %d", plan->device, dev);
+    unsigned int *flags = nullptr;
+    pgqa_status s = device_flags(&flags);
+    if (s != PGQA_OK) return s;
+    const pgqa_plan_config &c = plan->cfg;
+    e = launch_kv_append_rope(k_pool, v_pool, k, v, slot_mapping, positions, num_tokens, num_pages * c.page_size,
+                              c.num_kv_heads, c.head_dim, c.dtype, plan->rope_cs, c.rope_max_position, flags, true,
+                              reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append_rope launch");
+    return PGQA_OK;
+}
+
 pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     if (!out || !cfg) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
     *out = nullptr;
@@ -340,6 +368,13 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         return fail(PGQA_ERR_INVALID_ARG, "prefill_splits %d (0..8)", c.prefill_splits);
     if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
         return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 2 or 3)", c.pipeline_stages);
+    if (c.rope_theta < 0.0 || std::isnan(c.rope_theta)) return fail(PGQA_ERR_INVALID_ARG, "rope_theta %g", c.rope_theta);
+    if (c.rope_theta > 0.0) {
+        if (c.rope_max_position < 1 || c.rope_max_position > (1 << 24))
+            return fail(PGQA_ERR_INVALID_ARG, "rope_max_position %d outside [1, 2^24]", c.rope_max_position);
+        if (c.decode_kernel == PGQA_DECODE_CUDA_CORE)
+            return fail(PGQA_ERR_UNSUPPORTED, "RoPE runs on the tensor-core kernels");
+    }
 
     pgqa_plan *p = new (std::nothrow) pgqa_plan();
     if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
@@ -393,6 +428,13 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
         e = cudaMallocHost(&p->h_meta[i], meta);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->staged[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess && c.rope_theta > 0.0) {
+        // built once on the device (fp64 angles), complete before plan_create returns
+        const size_t bytes = sizeof(float2) * static_cast<size_t>(c.rope_max_position) * (c.head_dim / 2);
+        e = cudaMalloc(reinterpret_cast<void **>(&p->rope_cs), bytes);
+        if (e == cudaSuccess) e = launch_rope_table(p->rope_cs, c.rope_max_position, c.head_dim, c.rope_theta, 0);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(0);
     }
     if (e != cudaSuccess) {
         plan_free(p);
@@ -588,7 +630,18 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         const int64_t L = r1 - r0;
         // A fused append writes the request's last L key positions from the L new rows.
         if (L > n) fusable = false;
+        if (plan->rope_cs != nullptr && L > 0) {
+            // query rows sit at the request's last L key positions, all in the table
+            if (L > n)
+                return fail(PGQA_ERR_INVALID_ARG, "request %d: %lld query rows over %lld keys have no rotary position",
+                            b, static_cast<long long>(L), static_cast<long long>(n));
+            if (n > c.rope_max_position)
+                return fail(PGQA_ERR_INVALID_ARG, "request %d: key positions up to %lld exceed rope_max_position %d", b,
+                            static_cast<long long>(n - 1), c.rope_max_position);
+        }
         const int64_t nb = L <= n ? n - L : INT32_MAX;
+        // (Rows of tensor-core decode items therefore come from single-row requests: the
+        // decode kernel's fused append relies on at most one new row per item.)
         if (L > 1 && plan->kernel == PGQA_DECODE_TENSOR_CORE) {
             // A chunk of rows: tensor-core prefill tiles of 64 (row, head) pairs per kv head
             // (key slices are assigned below, once all tiles are known).
@@ -632,7 +685,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
             ns = n == 0 ? 1 : ceil_div(n, len);
             if (ns == 1) {
                 items.push_back({rw.page_base, 0, static_cast<int32_t>(n), rw.q_row, kvh, -1, rw.new_begin,
-                                 rw.new_row_base, rw.own_pos, 0, 0, 0});
+                                 rw.new_row_base, rw.own_pos, rw.own_pos, 0, 0});
                 continue;
             }
             if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_slots)
@@ -641,7 +694,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
                 items.push_back({rw.page_base, static_cast<int32_t>(s * len),
                                  static_cast<int32_t>(std::min<int64_t>(n, (s + 1) * len)), rw.q_row, kvh,
                                  slot + static_cast<int32_t>(s), rw.new_begin, rw.new_row_base,
-                                 s == ns - 1 ? rw.own_pos : -1, 0, 0, 0});
+                                 s == ns - 1 ? rw.own_pos : -1, rw.own_pos, 0, 0});
             tasks.push_back({rw.q_row, kvh, slot, static_cast<int32_t>(ns)});
             slot += static_cast<int>(ns);
             max_used = std::max<int>(max_used, static_cast<int>(ns));
@@ -828,6 +881,7 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
         pp.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
         pp.partial_o = plan->d_partial_o;
         pp.partial_lse = plan->d_partial_lse;
+        pp.rope_cs = plan->rope_cs;
         e = launch_prefill(c.head_dim, plan->group, c.dtype, *pk, *pv, pp, plan->n_prefill, true, st);
         if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     }
@@ -855,8 +909,11 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
     // With a prefill grid just launched, the decode grid runs beside it.
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
-    // The persistent schedule serves groups of up to 8 heads; wider groups run one CTA per item.
-    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0 && plan->group <= 8)
+    p.rope_cs = plan->rope_cs;
+    // The persistent schedule serves groups of up to 8 heads without RoPE; the rest run
+    // one CTA per item.
+    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0 && plan->group <= 8 &&
+                      plan->rope_cs == nullptr)
                          ? (c.decode_ctas > 0 ? c.decode_ctas : plan->num_sms)
                          : 0;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,

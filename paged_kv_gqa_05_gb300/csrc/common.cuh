@@ -28,7 +28,8 @@ struct alignas(16) WorkItem {
                            // (the request's last qo_len positions); INT32_MAX when it has none
     int32_t new_row_base;  // the new row of key position p is k_new[p + new_row_base]
     int32_t write_pos;     // key position whose new row this item stores into the pool, or -1
-    int32_t pad0, pad1, pad2;
+    int32_t q_pos;         // key position of the query row's own key: its rotary position
+    int32_t pad1, pad2;
 };
 static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
 
@@ -92,6 +93,8 @@ struct DecodeParams {
     int defer_wait;            // 1: launched right after an independent prefill grid of the same
                                // call; every older kernel is complete, so the dependency wait
                                // moves to the end (it only keeps completion order)
+    const float2 *rope_cs;     // rotary (cos, sin) table [positions][D/2]; null: q and new rows
+                               // are used as given
 };
 
 struct PrefillParams {
@@ -116,6 +119,7 @@ struct PrefillParams {
     int prefetch_pool;
     float *partial_o;          // split prefill rows: [slots, G, D]
     float *partial_lse;        // [slots, G] log2 domain
+    const float2 *rope_cs;     // as in DecodeParams
 };
 
 struct MergeParams {
@@ -144,6 +148,12 @@ cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bo
 cudaError_t launch_kv_append(void *k_pool, void *v_pool, const void *k, const void *v,
                              const int64_t *slot_mapping, int64_t num_tokens, int64_t num_slots,
                              int row_bytes, unsigned int *flags, bool pdl, cudaStream_t stream);
+cudaError_t launch_rope_table(float2 *cs, int max_position, int head_dim, double theta, cudaStream_t stream);
+cudaError_t launch_kv_append_rope(void *k_pool, void *v_pool, const void *k, const void *v,
+                                  const int64_t *slot_mapping, const int32_t *positions, int64_t num_tokens,
+                                  int64_t num_slots, int num_kv_heads, int head_dim, pgqa_dtype dtype,
+                                  const float2 *cs, int max_position, unsigned int *flags, bool pdl,
+                                  cudaStream_t stream);
 
 // Host helpers defined in api.cu.
 pgqa_status report(pgqa_status s, const char *msg);
@@ -331,6 +341,45 @@ __device__ __forceinline__ void named_bar_sync_id(int id, int count) {
 // it against __syncwarp and the barrier waits (which clobber memory).
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
+// The work item of this CTA into registers with three 16-byte loads that stay where
+// they are written.  A plain struct copy lets the compiler read each field at its first
+// use; a field first used after griddepcontrol.wait (a memory clobber) is then read
+// from global memory again there, putting a dependent load on the critical path.
+__device__ __forceinline__ WorkItem load_work_item(const WorkItem *src) {
+    static_assert(sizeof(WorkItem) == 48, "three 16-byte loads");
+    int32_t w[12];
+    const char *b = reinterpret_cast<const char *>(src);
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[4 * k]), "=r"(w[4 * k + 1]), "=r"(w[4 * k + 2]), "=r"(w[4 * k + 3])
+                     : "l"(b + 16 * k));
+    WorkItem it;
+    it.page_base = w[0];
+    it.tok_begin = w[1];
+    it.tok_end = w[2];
+    it.q_row = w[3];
+    it.kv_head = w[4];
+    it.out_slot = w[5];
+    it.new_begin = w[6];
+    it.new_row_base = w[7];
+    it.write_pos = w[8];
+    it.q_pos = w[9];
+    it.pad1 = w[10];
+    it.pad2 = w[11];
+    return it;
+}
+
+// A 16-byte shared-memory load the compiler keeps where it is written (not hoisted out
+// of the branch or loop that holds it).
+__device__ __forceinline__ float4 lds128_pinned(const void *p) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
 // Two packed 16-bit floats -> two fp32 (exact widening).
 template <typename T>
 __device__ __forceinline__ float2 widen2(uint32_t packed);
@@ -353,6 +402,55 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 narrow<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 template <>
 __device__ __forceinline__ __half narrow<__half>(float x) { return __float2half_rn(x); }
+
+// Two values rounded to T (nearest, ties to even) and packed, the first in the low half.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+           (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
+
+// Rotary embedding, rotate-half form: channel i < D/2 pairs with channel i + D/2 and
+// both turn by the angle whose (cos, sin) is entry i of the position's table row:
+//     lo' = lo cos - hi sin,   hi' = hi cos + lo sin,
+// in fp32 and rounded once to T.  lo packs channels i, i + 1; hi packs i + D/2,
+// i + D/2 + 1; cs = (cos_i, sin_i, cos_i+1, sin_i+1).  Every path that rotates a row
+// (q in registers, new K rows patched into tiles or stored into the pool) goes
+// through this one function, so a stored key matches the one attended bit for bit.
+template <typename T>
+__device__ __forceinline__ void rope_rotate2(uint32_t &lo, uint32_t &hi, float4 cs) {
+    const float2 a = widen2<T>(lo), b = widen2<T>(hi);
+    const float a0 = fmaf(a.x, cs.x, -__fmul_rn(b.x, cs.y));
+    const float a1 = fmaf(a.y, cs.z, -__fmul_rn(b.y, cs.w));
+    const float b0 = fmaf(b.x, cs.x, __fmul_rn(a.x, cs.y));
+    const float b1 = fmaf(b.y, cs.z, __fmul_rn(a.y, cs.w));
+    lo = pack2<T>(a0, a1);
+    hi = pack2<T>(b0, b1);
+}
+
+// 16-byte chunk `ch` (channels 8 ch .. 8 ch + 7) of the D-channel row at `row` with the
+// rotary embedding of table row `cs` applied; reads the chunk and its partner in the
+// other half.
+template <typename T, int D>
+__device__ __forceinline__ uint4 rope_chunk(const T *row, int ch, const float2 *cs) {
+    constexpr int HC = D / 16;  // chunks per half
+    const bool second = ch >= HC;
+    const int first = second ? ch - HC : ch;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row + first * 8));
+    const uint4 y = __ldg(reinterpret_cast<const uint4 *>(row + (first + HC) * 8));
+    const float4 *c = reinterpret_cast<const float4 *>(cs + first * 8);
+    uint32_t lo[4] = {x.x, x.y, x.z, x.w}, hi[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rope_rotate2<T>(lo[j], hi[j], __ldg(c + j));
+    return second ? make_uint4(hi[0], hi[1], hi[2], hi[3]) : make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
 
 #endif  // __CUDACC__
 

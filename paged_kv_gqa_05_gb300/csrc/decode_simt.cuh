@@ -390,6 +390,7 @@ cudaError_t launch_decode_g(const CUtensorMap &tm_k, const CUtensorMap &tm_v, co
 template <int D, typename T>
 cudaError_t launch_decode_dt(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const DecodeParams &p, int num_items, bool pdl, cudaStream_t stream) {
+    if (p.rope_cs != nullptr) return cudaErrorInvalidValue;  // rotary plans use the tensor-core kernel
     switch (group) {
         case 1: return launch_decode_g<D, 1, T>(tm_k, tm_v, p, num_items, pdl, stream);
         case 2: return launch_decode_g<D, 2, T>(tm_k, tm_v, p, num_items, pdl, stream);

@@ -103,7 +103,8 @@ struct TcCfg {
     static constexpr int DT = D / 16;                    // d m-tiles of the PV product
     static constexpr int KS = D / 16;                    // k-steps of the QK product
     static constexpr int OS = D + 4;                     // padded row stride (floats) of a warp's O
-    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4;
+    static constexpr int ROPE_BYTES = D * 4;             // one rotary table row: D/2 (cos, sin)
+    static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4 + ROPE_BYTES;
     static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
 };
 
@@ -114,11 +115,12 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * (decode_warp_tile(D) * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, int STAGES, int NH, typename T>
+template <int D, int STAGES, int NH, bool ROPE, typename T>
 __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 3 : 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p, int G) {
     // NH tiles of 8 query heads: G <= 8 * NH (NH = 2 serves groups of 9..16 heads).
+    // ROPE: q and the new K rows turn by the plan's rotary table (p.rope_cs).
     using C = TcCfg<D, STAGES>;
     constexpr int HP = 8 * NH;  // heads padded to whole n tiles
     using M = MmaType<T>;
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
     uint8_t *pipe = smem;
     const uint32_t bar0 = smem_addr(smem + C::PIPE_BYTES) + warp * C::ST * 8;
     int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PIPE_BYTES + C::BAR_BYTES);
+    float2 *rope_row = reinterpret_cast<float2 *>(smem + C::PIPE_BYTES + C::BAR_BYTES + kSlicePageCap * 4);
 
     if (smem_addr(smem) & 1023u) {  // the stage layout assumes this alignment of the window
         if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
@@ -142,7 +145,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
     // The work list and kv_indices are final once plan_update is enqueued (its
     // copy sits between any earlier writer and this kernel), so they are read
     // before the grid-dependency wait; q and the new rows only after it.
-    const WorkItem it = p.items[blockIdx.x];
+    const WorkItem it = load_work_item(p.items + blockIdx.x);
+    // The query row's rotary table row goes to shared memory.  The table is fixed since
+    // plan creation, so it is read before the dependency wait, in flight together with
+    // the page-table staging; the CTA barrier below publishes it.
+    float4 rope_part = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ROPE && threadIdx.x < D / 4)
+        rope_part = __ldg(reinterpret_cast<const float4 *>(p.rope_cs + static_cast<size_t>(it.q_pos) * (D / 2)) +
+                          threadIdx.x);
     const int ntiles = (it.tok_end - it.tok_begin + C::TW - 1) / C::TW;
     const int my_tiles = ntiles > warp ? (ntiles - warp + C::NW - 1) / C::NW : 0;
     const bool fused = p.k_new != nullptr;
@@ -157,6 +167,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
     }
     const SlicePages pages =
         stage_slice_pages(page_buf, p.kv_indices, it.page_base, it.tok_begin, it.tok_end, p.page_size);
+    if (ROPE && threadIdx.x < D / 4) reinterpret_cast<float4 *>(rope_row)[threadIdx.x] = rope_part;
     __syncthreads();
     const uint64_t policy = l2_evict_first_policy();
 
@@ -234,24 +245,72 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         }
     }
 
-    // Fused append: the first new row inside this slice is fetched now into the
-    // registers of the warp whose tile holds it (lanes [0, CH) carry K chunks,
-    // lanes [CH, 2CH) V chunks); any further new rows are read when met.
+    // Fused append.  A decode item of this kernel holds at most one of the call's new
+    // rows -- its row's own key, the last of the request (requests with several query
+    // rows run as prefill tiles) -- so the warp whose tile holds it fetches it now into
+    // registers (lanes [0, CH) carry K chunks, lanes [CH, 2CH) V chunks), patches it
+    // into that tile and stores it into the pool; nothing else of the append sits in
+    // the tile loop.
     int pf_pos = -1;
     uint4 pf = make_uint4(0u, 0u, 0u, 0u);
     const bool row_lane = lane < 2 * CH;
     const int rch = lane % CH;
     const bool rv = lane >= CH;
+    auto new_row = [&](int pos) -> const T * {
+        return static_cast<const T *>(rv ? p.v_new : p.k_new) +
+               (static_cast<size_t>(pos + it.new_row_base) * p.num_kv_heads + it.kv_head) * D;
+    };
     auto new_row_chunk = [&](int pos) -> uint4 {
-        const T *src = static_cast<const T *>(rv ? p.v_new : p.k_new) +
-                       (static_cast<size_t>(pos + it.new_row_base) * p.num_kv_heads + it.kv_head) * D + rch * 8;
-        return __ldg(reinterpret_cast<const uint4 *>(src));
+        return __ldg(reinterpret_cast<const uint4 *>(new_row(pos) + rch * 8));
+    };
+    // With RoPE the prefetched chunk stays raw until first used, so the owning warp does
+    // not wait on it here.  Rotating it is warp-collective: the partner half of a K
+    // chunk comes from lane ^ CH/2 and the table entries from shared memory (the new
+    // row is the query row's own key, so its position is the query row's).
+    bool pf_rot = !ROPE;
+    auto rotate_pf = [&]() {
+        if (pf_rot) return;
+        pf_rot = true;
+        uint4 y;
+        y.x = __shfl_xor_sync(0xffffffffu, pf.x, CH / 2);
+        y.y = __shfl_xor_sync(0xffffffffu, pf.y, CH / 2);
+        y.z = __shfl_xor_sync(0xffffffffu, pf.z, CH / 2);
+        y.w = __shfl_xor_sync(0xffffffffu, pf.w, CH / 2);
+        if (rv) return;  // V chunks (and idle lanes) keep theirs
+        const bool second = rch >= CH / 2;
+        const int first = second ? rch - CH / 2 : rch;
+        uint32_t lo[4] = {pf.x, pf.y, pf.z, pf.w}, hi[4] = {y.x, y.y, y.z, y.w};
+        if (second) {
+            lo[0] = y.x; lo[1] = y.y; lo[2] = y.z; lo[3] = y.w;
+            hi[0] = pf.x; hi[1] = pf.y; hi[2] = pf.z; hi[3] = pf.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rope_rotate2<T>(lo[j], hi[j], lds128_pinned(rope_row + first * 8 + 2 * j));
+        pf = second ? make_uint4(hi[0], hi[1], hi[2], hi[3]) : make_uint4(lo[0], lo[1], lo[2], lo[3]);
     };
     if (fused) {
         const int nb = max(it.new_begin, it.tok_begin);
         if (nb < it.tok_end && ((nb - it.tok_begin) / C::TW) % C::NW == warp) {
             pf_pos = nb;
             if (row_lane) pf = new_row_chunk(nb);
+            // The plan only builds items whose new row is the query row's own key.
+            if (ROPE && nb != it.q_pos && lane == 0) atomicOr(p.flags, PGQA_FLAG_ROPE_POSITION);
+        }
+    }
+
+    if (ROPE) {
+        // Rotary embedding of q at its row's position: channels 16 ks + 2 c4 (+1, +8, +9)
+        // of the first half sit in k-step ks, their partners (+ D/2) in k-step ks + KS/2
+        // of the same thread.
+#pragma unroll
+        for (int ks = 0; ks < C::KS / 2; ++ks) {
+            const float4 c0 = lds128_pinned(rope_row + ks * 16 + 2 * c4);
+            const float4 c1 = lds128_pinned(rope_row + ks * 16 + 2 * c4 + 8);
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+                rope_rotate2<T>(qf[ks][nh][0], qf[ks + C::KS / 2][nh][0], c0);
+                rope_rotate2<T>(qf[ks][nh][1], qf[ks + C::KS / 2][nh][1], c1);
+            }
         }
     }
 
@@ -287,19 +346,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         const uint32_t kb = smem_addr(kp);
         const uint32_t vb = kb + C::TILE_BYTES;
 
-        // ---- fused append: rows of this call's new tokens replace what the pool held
+        // ---- fused append: the call's new row replaces what the pool held at its position
         bool patched = false;
-        if (fused) {
-            const int nb = max(it.new_begin, tb);
-            if (nb < tb + nvalid) {  // warp-uniform
-                for (int pos = nb; pos < tb + nvalid; ++pos) {
-                    const uint4 val = (pos == pf_pos) ? pf : (row_lane ? new_row_chunk(pos) : pf);
-                    if (row_lane)
-                        *reinterpret_cast<uint4 *>(kp + (rv ? C::TILE_BYTES : 0) + tile_off<D>(pos - tb, rch)) = val;
-                }
-                patched = true;
-                __syncwarp();
-            }
+        if (pf_pos >= tb && pf_pos < tb + nvalid) {  // warp-uniform
+            rotate_pf();
+            if (row_lane) *reinterpret_cast<uint4 *>(kp + (rv ? C::TILE_BYTES : 0) + tile_off<D>(pf_pos - tb, rch)) = pf;
+            patched = true;
+            __syncwarp();
         }
 
         // ---- S^T = K . Q^T for the tile's m-tiles (rows = tokens)
@@ -437,7 +490,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         const int nb = max(it.new_begin, it.tok_begin);
         const bool held = nb < it.tok_end && nb == pos;
         const int writer = held ? ((nb - it.tok_begin) / C::TW) % C::NW : 0;
-        if (warp == writer && row_lane) {
+        if (warp == writer && held) rotate_pf();  // warp-collective, before the lanes split
+        // (with RoPE the written row is always the held one: see the fused-append note above)
+        if (warp == writer && row_lane && (held || !ROPE)) {
             const int64_t page = (pos >= it.tok_begin && pos < it.tok_end)
                                      ? pages(pos, p.page_size)
                                      : p.kv_indices[it.page_base + pos / p.page_size];
@@ -553,7 +608,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
 }
 
 // Raises the kernel's dynamic shared-memory limit once per device.
-template <int D, int STAGES, int NH, typename T>
+template <int D, int STAGES, int NH, bool ROPE, typename T>
 cudaError_t configure_decode_tc() {
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -561,19 +616,19 @@ cudaError_t configure_decode_tc() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcCfg<D, STAGES>::SMEM_BYTES);
+        e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, ROPE, T>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D, STAGES>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     return cudaSuccess;
 }
 
-template <int D, int STAGES, int NH, typename T>
+template <int D, int STAGES, int NH, bool ROPE, typename T>
 cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
                                 int num_items, bool pdl, cudaStream_t stream) {
     using C = TcCfg<D, STAGES>;
-    cudaError_t e = configure_decode_tc<D, STAGES, NH, T>();
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, ROPE, T>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
@@ -585,16 +640,25 @@ cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtens
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, T>, tm_k, tm_v, p, group);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, ROPE, T>, tm_k, tm_v, p, group);
+}
+
+// The rotary variant is a separate instantiation, so plans without RoPE run code
+// with no trace of it (timed: the runtime branch alone cost 3 % on 128 x 301).
+template <int D, int STAGES, int NH, typename T>
+cudaError_t launch_decode_tc_r(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
+                               int num_items, bool pdl, cudaStream_t stream) {
+    return p.rope_cs != nullptr ? launch_decode_tc_st<D, STAGES, NH, true, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                                : launch_decode_tc_st<D, STAGES, NH, false, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 // CTAs of one per-item kernel variant resident on an SM at once (registers and
 // shared memory), the slot count of the split heuristic.
 template <int D, int STAGES, int NH, typename T>
 cudaError_t decode_tc_blocks_per_sm_st(int *blocks) {
-    cudaError_t e = configure_decode_tc<D, STAGES, NH, T>();
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, false, T>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_tc_kernel<D, STAGES, NH, T>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_tc_kernel<D, STAGES, NH, false, T>,
                                                          TcCfg<D, STAGES>::NW * 32, TcCfg<D, STAGES>::SMEM_BYTES);
 }
 
@@ -609,10 +673,10 @@ template <int D, typename T>
 cudaError_t launch_decode_tc(int stages, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const DecodeParams &p, int num_items, bool pdl, cudaStream_t stream) {
     if (group > 8)
-        return stages == 3 ? launch_decode_tc_st<D, 3, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
-                           : launch_decode_tc_st<D, 2, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
-    return stages == 3 ? launch_decode_tc_st<D, 3, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
-                       : launch_decode_tc_st<D, 2, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
+        return stages == 3 ? launch_decode_tc_r<D, 3, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                           : launch_decode_tc_r<D, 2, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return stages == 3 ? launch_decode_tc_r<D, 3, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                       : launch_decode_tc_r<D, 2, 1, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 }  // namespace pgqa

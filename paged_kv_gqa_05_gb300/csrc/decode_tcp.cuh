@@ -502,6 +502,7 @@ template <int D, typename T>
 cudaError_t launch_decode_tcp(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
                               int num_items, int grid, bool pdl, cudaStream_t stream) {
     if (group < 1 || group > 8) return cudaErrorInvalidValue;  // one 8-head n tile
+    if (p.rope_cs != nullptr) return cudaErrorInvalidValue;    // rotary plans run one CTA per item
     return launch_decode_tcp_st<D, D == 64 ? 3 : 2, T>(group, tm_k, tm_v, p, num_items, grid, pdl, stream);
 }
 

@@ -47,7 +47,7 @@ __device__ __forceinline__ uint32_t ptile_off(int r, int c) {
     return (c >> 3) * (PrefillCfg<D>::HALF_BYTES) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, typename T>
+template <int D, bool ROPE, typename T>
 __global__ void __launch_bounds__(128, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const PrefillParams p, int G) {
@@ -73,6 +73,15 @@ __global__ void __launch_bounds__(128, 2)
     const int ntiles = key_end > key_begin ? (key_end - key_begin + C::KT - 1) / C::KT : 0;
     const bool fused = p.k_new != nullptr;
     const int new_begin = it.n_keys - it.rows;   // the chunk's own keys (a fused call supplies them)
+    // Chunk ch of the new K (rotated at its key position when the plan uses RoPE) or V
+    // row of key position pos >= new_begin.
+    auto new_chunk = [&](bool isv, int pos, int ch) -> uint4 {
+        const T *row = static_cast<const T *>(isv ? p.v_new : p.k_new) +
+                       (static_cast<size_t>(it.q_row0 + pos - new_begin) * p.num_kv_heads + it.kv_head) * D;
+        if (ROPE && !isv)
+            return rope_chunk<T, D>(row, ch, p.rope_cs + static_cast<size_t>(pos) * (D / 2));
+        return __ldg(reinterpret_cast<const uint4 *>(row + ch * 8));
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::ST; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -126,6 +135,7 @@ __global__ void __launch_bounds__(128, 2)
     // This lane's two pair rows: r = 0 -> pair m0 + 16 warp + g8, r = 1 -> + 8.
     int limit[2];       // last admissible key of the row (< 0: none)
     bool valid_row[2];  // the pair is a real (row, head) of the request
+    int qi[2];          // the pair's row within the request
     uint32_t qa[C::KS][4];
     {
         const T *qb[2];
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(128, 2)
             const int m = it.pair0 + warp * 16 + g8 + 8 * r;
             const int i = m / G, h = m - (m / G) * G;
             const bool valid = i < it.rows;
+            qi[r] = i;
             valid_row[r] = valid;
             limit[r] = !valid ? -1 : (p.causal ? it.n_keys - it.rows + i : it.n_keys - 1);
             limit[r] = min(limit[r], key_end - 1);  // keys of this CTA's slice only
@@ -148,6 +159,22 @@ __global__ void __launch_bounds__(128, 2)
             qa[ks][1] = qb[1] ? __ldg(reinterpret_cast<const uint32_t *>(qb[1] + d0)) : 0u;
             qa[ks][2] = qb[0] ? __ldg(reinterpret_cast<const uint32_t *>(qb[0] + d0 + 8)) : 0u;
             qa[ks][3] = qb[1] ? __ldg(reinterpret_cast<const uint32_t *>(qb[1] + d0 + 8)) : 0u;
+        }
+    }
+    if (ROPE) {
+        // Rotary embedding of each real row at its position new_begin + i: channels
+        // 16 ks + 2 c4 (+1, +8, +9) pair with the same channels of k-step ks + KS/2.
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (!valid_row[r]) continue;
+            const float2 *cs = p.rope_cs + static_cast<size_t>(new_begin + qi[r]) * (D / 2);
+#pragma unroll
+            for (int ks = 0; ks < C::KS / 2; ++ks) {
+                const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cs + ks * 16 + 2 * c4));
+                const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cs + ks * 16 + 2 * c4 + 8));
+                rope_rotate2<T>(qa[ks][r], qa[ks + C::KS / 2][r], c0);
+                rope_rotate2<T>(qa[ks][2 + r], qa[ks + C::KS / 2][2 + r], c1);
+            }
         }
     }
     // Largest / smallest admissible key over the warp's real rows (rows grow with m).
@@ -190,11 +217,8 @@ __global__ void __launch_bounds__(128, 2)
                 const int ch = rem - (isv ? CH : 0);
                 const int pos = t0 + r;
                 if (pos < new_begin) continue;
-                const T *src = static_cast<const T *>(isv ? p.v_new : p.k_new) +
-                               (static_cast<size_t>(it.q_row0 + pos - new_begin) * p.num_kv_heads + it.kv_head) * D +
-                               ch * 8;
                 *reinterpret_cast<uint4 *>(kp + (isv ? C::TILE_BYTES : 0) + ptile_off<D>(r, ch)) =
-                    __ldg(reinterpret_cast<const uint4 *>(src));
+                    new_chunk(isv, pos, ch);
             }
             patched = true;
             __syncthreads();
@@ -325,11 +349,9 @@ __global__ void __launch_bounds__(128, 2)
                 atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
                 continue;
             }
-            const T *src = static_cast<const T *>(isv ? p.v_new : p.k_new) +
-                           (static_cast<size_t>(it.q_row0 + i) * p.num_kv_heads + it.kv_head) * D + ch * 8;
             T *dst = static_cast<T *>(isv ? p.v_pool : p.k_pool) +
                      ((page * p.page_size + pos % p.page_size) * p.num_kv_heads + it.kv_head) * D + ch * 8;
-            *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(src));
+            *reinterpret_cast<uint4 *>(dst) = new_chunk(isv, pos, ch);
         }
     }
 
@@ -368,11 +390,11 @@ __global__ void __launch_bounds__(128, 2)
     }
 }
 
-template <int D, typename T>
-cudaError_t launch_prefill_tc(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const PrefillParams &p,
-                              int num_items, bool pdl, cudaStream_t stream) {
+template <int D, bool ROPE, typename T>
+cudaError_t launch_prefill_tc_r(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const PrefillParams &p,
+                                int num_items, bool pdl, cudaStream_t stream) {
     using C = PrefillCfg<D>;
-    auto kern = prefill_tc_kernel<D, T>;
+    auto kern = prefill_tc_kernel<D, ROPE, T>;
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -394,6 +416,14 @@ cudaError_t launch_prefill_tc(int group, const CUtensorMap &tm_k, const CUtensor
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p, group);
+}
+
+// Plans without RoPE run an instantiation with no trace of it.
+template <int D, typename T>
+cudaError_t launch_prefill_tc(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const PrefillParams &p,
+                              int num_items, bool pdl, cudaStream_t stream) {
+    return p.rope_cs != nullptr ? launch_prefill_tc_r<D, true, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
+                                : launch_prefill_tc_r<D, false, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 }  // namespace pgqa

@@ -237,6 +237,16 @@ def make(name: str, seed: int = 0) -> Workload:
     return WORKLOADS[name](seed)
 
 
+def row_positions(w: Workload) -> np.ndarray:
+    """Key position of each query row's own token: the last L positions of a request
+    with N keys and L rows are N - L .. N - 1 (int32, one per row)."""
+    pos = np.zeros(w.rows, np.int32)
+    for b in range(w.batch):
+        r0, r1 = (b, b + 1) if w.qo_indptr is None else (int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
+        pos[r0:r1] = int(w.kv_lens[b]) - (r1 - r0) + np.arange(r1 - r0)
+    return pos
+
+
 def algorithmic_bytes(w: Workload, out_elem_bytes: int = 2) -> dict:
     """Bytes a paged decode call must move at minimum: the K/V rows attended
     (counted once per KV head even though a query group shares them), q, the

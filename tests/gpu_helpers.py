@@ -29,6 +29,27 @@ def oracle_outputs(w: W.Workload, appended: bool = True):
                                w.dtype, qo_indptr=w.qo_indptr, causal=w.causal, nthreads=NTHREADS)
 
 
+def new_rows_for_query_rows(w: W.Workload, seed: int = 7):
+    """One new K/V row per query row: request b's rows land on its last qo_len key
+    positions.  Returns (k_new, v_new, flat slots) and NaN-poisons those slots."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = W.TORCH_DTYPES[w.dtype]
+    k_new = torch.randn(w.rows, w.num_kv_heads, w.head_dim, generator=gen).to(dt)
+    v_new = torch.randn(w.rows, w.num_kv_heads, w.head_dim, generator=gen).to(dt)
+    slots = np.zeros(w.rows, np.int64)
+    for b in range(w.batch):
+        r0, r1 = (b, b + 1) if w.qo_indptr is None else (int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
+        n = int(w.kv_lens[b])
+        for i, r in enumerate(range(r0, r1)):
+            pos = n - (r1 - r0) + i
+            page = int(w.kv_indices[w.kv_indptr[b] + pos // w.page_size])
+            slots[r] = page * w.page_size + pos % w.page_size
+    w.k_pool.view(-1, w.num_kv_heads, w.head_dim)[torch.from_numpy(slots)] = float("nan")
+    w.v_pool.view(-1, w.num_kv_heads, w.head_dim)[torch.from_numpy(slots)] = float("nan")
+    w.k_new, w.v_new, w.slot_mapping = k_new, v_new, slots
+    return k_new, v_new, slots
+
+
 def to_device(w: W.Workload, device="cuda"):
     d = {
         "q": w.q.to(device),

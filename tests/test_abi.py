@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.pgqa_abi_version() == 1
+    assert lib.pgqa_abi_version() == 2
     for code in range(7):
         assert lib.pgqa_status_string(code)
 
@@ -65,6 +65,24 @@ def test_argument_checks_before_device(lib):
     assert lib.pgqa_kv_append(None, None, 1, 12, 2, 64, 0, None, None, None, 1, None) == 2
     assert lib.pgqa_plan_update(None, None, None, None, 0, None, None, 0, 0, None) == 1
     assert lib.pgqa_run(None, None, None, None, None, 0, None, 0.0, None) == 1
+    # RoPE configuration checks, also before any device call
+    PC = __import__("paged_kv_gqa_05_gb300").binding.PlanConfig
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0,
+                                                                  4096, -1.0))) == 1  # negative theta
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0,
+                                                                  0, 1.0e6))) == 1  # no positions
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 2, 0, 0, 0,
+                                                                  4096, 1.0e6))) == 2  # CUDA-core kernel
+    assert lib.pgqa_kv_append_rope(None, None, None, 1, None, None, None, None, 1, None) == 1
+
+
+def test_plan_config_layout():
+    """The ctypes mirror of pgqa_plan_config: natural C alignment, rope_theta last."""
+    from paged_kv_gqa_05_gb300 import binding
+    PC = binding.PlanConfig
+    assert PC.max_q_rows.offset == 24 and PC.decode_ctas.offset == 56
+    assert PC.rope_max_position.offset == 60 and PC.rope_theta.offset == 64
+    assert ctypes.sizeof(PC) == 72
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -12,27 +12,6 @@ import gpu_helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def new_rows_for_query_rows(w: W.Workload, seed: int = 7):
-    """One new K/V row per query row: request b's rows land on its last qo_len key
-    positions.  Returns (k_new, v_new, flat slots) and NaN-poisons those slots."""
-    gen = torch.Generator().manual_seed(seed)
-    dt = W.TORCH_DTYPES[w.dtype]
-    k_new = torch.randn(w.rows, w.num_kv_heads, w.head_dim, generator=gen).to(dt)
-    v_new = torch.randn(w.rows, w.num_kv_heads, w.head_dim, generator=gen).to(dt)
-    slots = np.zeros(w.rows, np.int64)
-    for b in range(w.batch):
-        r0, r1 = (b, b + 1) if w.qo_indptr is None else (int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
-        n = int(w.kv_lens[b])
-        for i, r in enumerate(range(r0, r1)):
-            pos = n - (r1 - r0) + i
-            page = int(w.kv_indices[w.kv_indptr[b] + pos // w.page_size])
-            slots[r] = page * w.page_size + pos % w.page_size
-    w.k_pool.view(-1, w.num_kv_heads, w.head_dim)[torch.from_numpy(slots)] = float("nan")
-    w.v_pool.view(-1, w.num_kv_heads, w.head_dim)[torch.from_numpy(slots)] = float("nan")
-    w.k_new, w.v_new, w.slot_mapping = k_new, v_new, slots
-    return k_new, v_new, slots
-
-
 def fused_gpu(w, pool_stable=False, out_dtype=torch.float32, **plan_opts):
     dev = H.to_device(w)
     plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dev["q"].dtype,
@@ -74,7 +53,7 @@ def test_fused_decode_step(opts, pool_stable):
 def test_fused_shapes(head_dim, page_size, dtype, heads):
     w = W.custom("fz", [1, 2, 17, 33, 200, 700], page_size, heads, 2, head_dim, dtype, 64,
                  seed=head_dim + page_size + heads)
-    new_rows_for_query_rows(w)
+    H.new_rows_for_query_rows(w)
     ro, rl = H.oracle_outputs(w)
     out, lse, dev, _ = fused_gpu(w, split_tokens=64)
     H.compare(out, lse, ro, rl, f"fused d{head_dim} ps{page_size} {dtype} Hq{heads}")
@@ -86,7 +65,7 @@ def test_fused_multi_row(causal):
     """A chunk of L query rows per request appends L rows (the ragged step)."""
     w = W.custom("fzr", [40, 7, 300, 64], 16, 14, 2, 64, "bf16", 64, seed=11, qo_lens=[13, 1, 5, 64],
                  causal=causal)
-    new_rows_for_query_rows(w)
+    H.new_rows_for_query_rows(w)
     ro, rl = H.oracle_outputs(w)
     out, lse, dev, _ = fused_gpu(w, split_tokens=64)
     H.compare(out, lse, ro, rl, f"fused multi-row causal={causal}")
