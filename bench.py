@@ -382,7 +382,10 @@ def run_ours(args, rank, world, local):
         launch_bytes = b["attention_per_layer"]
         timing_note = "run()-only CUDA graph over the layer pools, events on the launch stream"
     achieved = launch_bytes / per_launch_s / 1e9
-    traffic = profiled_traffic(args.workload) if args.decode_kernel != "cuda_core" else None
+    # the committed counters describe the default launch of this workload only
+    default_launch = (args.decode_kernel != "cuda_core" and not args.rope_theta and not args.split_tokens and
+                      not args.max_splits and not args.stages and not args.decode_ctas and not args.ctas_per_sm)
+    traffic = profiled_traffic(args.workload) if default_launch else None
     e2e_value = sum_over_ranks(b["per_step"] * args.steps, world, device) / t_e2e / 1e9
 
     result = {
