@@ -29,7 +29,7 @@ struct TcpCfg {
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int PIPE_BYTES = NW * ST * STAGE_BYTES;
-    static constexpr int BAR_BYTES = NW * ST * 8;
+    static constexpr int BAR_BYTES = (NW * ST * 8 + 15) / 16 * 16;  // mbarriers, padded to 16 bytes
     static constexpr int DT = D / 16;
     static constexpr int KS = D / 16;
     static constexpr int OS = D + 4;
