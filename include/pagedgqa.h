@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define PGQA_ABI_VERSION 2
+#define PGQA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define PGQA_API __attribute__((visibility("default")))
@@ -137,7 +137,14 @@ typedef struct pgqa_plan_config {
     int rope_max_position; /* RoPE plans: positions 0 .. rope_max_position - 1 are valid */
     double rope_theta;    /* > 0: rotary position embedding with this base (see below);
                              0: none */
+    int prefill_kernel;   /* requests with several query rows: PGQA_PREFILL_AUTO (the
+                             tcgen05 kernel), PGQA_PREFILL_TCGEN05 or PGQA_PREFILL_MMA_SYNC
+                             (kept as a measured alternative) */
 } pgqa_plan_config;
+
+#define PGQA_PREFILL_AUTO 0
+#define PGQA_PREFILL_TCGEN05 1
+#define PGQA_PREFILL_MMA_SYNC 2
 
 /*
  * Rotary position embedding (RoPE).  The "flashlet" README lists a RoPE fusion

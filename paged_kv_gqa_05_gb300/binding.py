@@ -48,7 +48,7 @@ class PlanConfig(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int), ("decode_kernel", ctypes.c_int),
                 ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
                 ("decode_ctas", ctypes.c_int), ("rope_max_position", ctypes.c_int),
-                ("rope_theta", ctypes.c_double)]
+                ("rope_theta", ctypes.c_double), ("prefill_kernel", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -103,7 +103,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_plan_destroy.argtypes = [_vp]
     lib.pgqa_plan_get_info.restype = ctypes.c_int
     lib.pgqa_plan_get_info.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
-    if lib.pgqa_abi_version() != 2:
+    if lib.pgqa_abi_version() != 3:
         raise RuntimeError("libpagedgqa.so ABI version mismatch")
     _lib = lib
     return lib
@@ -185,14 +185,17 @@ def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: 
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
                 pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0,
-                rope_theta: float = 0.0, rope_max_position: int = 0) -> int:
+                rope_theta: float = 0.0, rope_max_position: int = 0, prefill_kernel: str = "auto") -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
     decode_kernel: "auto" | "tensor_core" | "cuda_core"; rope_theta > 0 turns on the
-    rotary embedding of q and the appended K rows (positions < rope_max_position)."""
+    rotary embedding of q and the appended K rows (positions < rope_max_position);
+    prefill_kernel: "auto" | "tcgen05" | "mma_sync"."""
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
+    pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
     cfg = PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                      max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
-                     pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta))
+                     pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta),
+                     pf_kinds[prefill_kernel])
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value

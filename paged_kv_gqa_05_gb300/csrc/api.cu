@@ -41,19 +41,19 @@ cudaError_t decode_blocks_per_sm(int stages, int head_dim, int group, pgqa_dtype
                                 : (head_dim == 64 ? decode_blocks_per_sm_fp16_d64 : decode_blocks_per_sm_fp16_d128);
     return f(stages, group, blocks);
 }
-using PrefillLauncher = cudaError_t (*)(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int,
-                                         bool, cudaStream_t);
-cudaError_t launch_prefill_bf16_d64(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
-cudaError_t launch_prefill_bf16_d128(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
-cudaError_t launch_prefill_fp16_d64(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
-cudaError_t launch_prefill_fp16_d128(int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+using PrefillLauncher = cudaError_t (*)(int, int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &,
+                                         int, bool, cudaStream_t);
+cudaError_t launch_prefill_bf16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_bf16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_fp16_d64(int, int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
+cudaError_t launch_prefill_fp16_d128(int, int, const CUtensorMap &, const CUtensorMap &, const PrefillParams &, int, bool, cudaStream_t);
 
-cudaError_t launch_prefill(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_prefill(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                            const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
                            cudaStream_t stream) {
     PrefillLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_prefill_bf16_d64 : launch_prefill_bf16_d128)
                                            : (head_dim == 64 ? launch_prefill_fp16_d64 : launch_prefill_fp16_d128);
-    return f(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return f(kind, group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa
 
@@ -172,6 +172,8 @@ struct pgqa_plan {
     int ctas_per_sm = 0;     // CTA slots per SM for 2-stage plans (the most of any variant)
     int slots_per_sm[4] = {0, 0, 0, 0};  // by pipeline depth (2 or 3): resident decode CTAs per SM
     int kernel = PGQA_DECODE_TENSOR_CORE;
+    int prefill_kind = PGQA_PREFILL_TCGEN05;  // prefill-segment kernel
+    int prefill_pairs = 128;                  // (row, head) pairs per prefill tile of that kernel
     int stages = 2;     // per-warp pipeline depth of the tensor-core kernel (chosen per plan_update)
     int max_items = 0;  // capacity of the work list and of the partial slots
     int max_tasks = 0;
@@ -364,6 +366,8 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
         return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
     if (c.decode_ctas < -1) return fail(PGQA_ERR_INVALID_ARG, "decode_ctas %d", c.decode_ctas);
+    if (c.prefill_kernel < PGQA_PREFILL_AUTO || c.prefill_kernel > PGQA_PREFILL_MMA_SYNC)
+        return fail(PGQA_ERR_INVALID_ARG, "prefill_kernel %d", c.prefill_kernel);
     if (c.prefill_splits < 0 || c.prefill_splits > 8)
         return fail(PGQA_ERR_INVALID_ARG, "prefill_splits %d (0..8)", c.prefill_splits);
     if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
@@ -384,6 +388,8 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->box_rows = std::min(c.page_size, p->tile);
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
     p->stages = c.pipeline_stages == 3 ? 3 : 2;
+    p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_MMA_SYNC ? PGQA_PREFILL_MMA_SYNC : PGQA_PREFILL_TCGEN05;
+    p->prefill_pairs = p->prefill_kind == PGQA_PREFILL_MMA_SYNC ? 64 : 128;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     // CTA slots of the split heuristic, unless the caller fixes them: the resident CTAs
@@ -643,12 +649,13 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         // (Rows of tensor-core decode items therefore come from single-row requests: the
         // decode kernel's fused append relies on at most one new row per item.)
         if (L > 1 && plan->kernel == PGQA_DECODE_TENSOR_CORE) {
-            // A chunk of rows: tensor-core prefill tiles of 64 (row, head) pairs per kv head
-            // (key slices are assigned below, once all tiles are known).
+            // A chunk of rows: tensor-core prefill tiles of prefill_pairs (row, head) pairs per
+            // kv head (key slices are assigned below, once all tiles are known).
             const int G = plan->group;
+            const int mp = plan->prefill_pairs;
             for (int kvh = 0; kvh < c.num_kv_heads; ++kvh)
-                for (int64_t m0 = 0; m0 < L * G; m0 += 64) {
-                    const int64_t i_last = std::min<int64_t>(L - 1, (m0 + 63) / G);
+                for (int64_t m0 = 0; m0 < L * G; m0 += mp) {
+                    const int64_t i_last = std::min<int64_t>(L - 1, (m0 + mp - 1) / G);
                     int64_t kend = causal ? n - L + i_last + 1 : n;
                     kend = std::max<int64_t>(0, std::min<int64_t>(n, kend));
                     prefill.push_back({kv_indptr[b], 0, static_cast<int32_t>(kend), static_cast<int32_t>(r0),
@@ -882,7 +889,8 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
         pp.partial_o = plan->d_partial_o;
         pp.partial_lse = plan->d_partial_lse;
         pp.rope_cs = plan->rope_cs;
-        e = launch_prefill(c.head_dim, plan->group, c.dtype, *pk, *pv, pp, plan->n_prefill, true, st);
+        e = launch_prefill(plan->prefill_kind, c.head_dim, plan->group, c.dtype, *pk, *pv, pp, plan->n_prefill, true,
+                           st);
         if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     }
     if (plan->n_items > 0) {

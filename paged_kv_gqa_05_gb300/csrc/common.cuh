@@ -140,7 +140,7 @@ struct MergeParams {
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items, int grid,
                           bool pdl, cudaStream_t stream);
-cudaError_t launch_prefill(int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
+cudaError_t launch_prefill(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                            const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
                            cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams &p, int num_tasks, int max_splits, bool pdl,

@@ -1,10 +1,11 @@
 // Split-KV decode partial kernels instantiated for fp16, head_dim 64: the
 // tensor-core kernel (any group width up to 16; one CTA per work item with 2- or
 // 3-stage pipelines, or the persistent form), the CUDA-core kernel (groups 1..8) and
-// the prefill-segment kernel.
+// the prefill-segment kernels (tcgen05, and the mma.sync form).
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
 #include "decode_tcp.cuh"
+#include "prefill_t5.cuh"
 #include "prefill_tc.cuh"
 
 namespace pgqa {
@@ -21,8 +22,9 @@ cudaError_t decode_blocks_per_sm_fp16_d64(int stages, int group, int *blocks) {
     return decode_tc_blocks_per_sm<64, __half>(stages, group, blocks);
 }
 
-cudaError_t launch_prefill_fp16_d64(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+cudaError_t launch_prefill_fp16_d64(int kind, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                       const PrefillParams &p, int num_items, bool pdl, cudaStream_t stream) {
-    return launch_prefill_tc<64, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    if (kind == PGQA_PREFILL_MMA_SYNC) return launch_prefill_tc<64, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return launch_prefill_t5<64, __half>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 }  // namespace pgqa

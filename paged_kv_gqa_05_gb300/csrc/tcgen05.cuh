@@ -1,0 +1,120 @@
+// Thin inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) and their
+// tensor memory (TMEM), cta_group::1 forms only.
+//
+// Encodings used by this library (checked on GB300 against a CPU matrix product
+// for K-major and MN-major operands, N = 64 and 128, A from shared memory and
+// from TMEM):
+//   shared-memory matrix descriptor (64 bit): start address >> 4 in bits [0,14),
+//     leading byte offset >> 4 in [16,30), stride byte offset >> 4 in [32,46),
+//     version 1 in [46,48), layout type in [61,64) (2 = 128-byte swizzle).
+//     128-byte-swizzled K-major tile (rows of 64 16-bit values = 128 bytes, 8-row
+//     atoms of 1024 bytes): stride offset 1024; a 16-wide k step adds 32 bytes to
+//     the start address.  128-byte-swizzled MN-major tile (K rows of 64 MN values):
+//     stride offset 1024 (between 8-row K groups), leading offset = distance between
+//     consecutive 64-wide MN blocks; a 16-deep k step adds 2048 bytes.
+//   instruction descriptor (kind::f16, 32 bit): D format in [4,6) (1 = f32), A and
+//     B formats in [7,10) and [10,13) (0 = f16, 1 = bf16), B major-ness at bit 16
+//     (1 = MN-major), N >> 3 in [17,23), M >> 4 in [24,29).
+//   TMEM address: lane in bits [16,32), column in [0,16).  The accumulator of an
+//     M = 128 product holds row i in lane i; warp w of a CTA reaches lanes
+//     [32 (w % 4), 32 (w % 4) + 32).  A 16-bit A operand in TMEM packs two
+//     k-adjacent values per 32-bit column, the lower k in the low half.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace pgqa {
+namespace t5 {
+
+__host__ __device__ constexpr uint64_t smem_desc_bits(uint32_t lbo, uint32_t sbo) {
+    return (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint64_t bits) {
+    return bits | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+}
+
+template <typename T>
+struct Fmt;
+template <>
+struct Fmt<__nv_bfloat16> {
+    static constexpr uint32_t code = 1;
+};
+template <>
+struct Fmt<__half> {
+    static constexpr uint32_t code = 0;
+};
+
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (Fmt<T>::code << 7) | (Fmt<T>::code << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Allocation (one whole warp), result written to shared memory.
+__device__ __forceinline__ void alloc(uint32_t slot_saddr, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] . B[smem]  (one thread issues)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+// Arrive on an mbarrier once every earlier tcgen05.mma of this thread has completed.
+__device__ __forceinline__ void commit(uint32_t bar_saddr) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_saddr)
+                 : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace t5
+}  // namespace pgqa

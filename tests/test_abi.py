@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.pgqa_abi_version() == 2
+    assert lib.pgqa_abi_version() == 3
     for code in range(7):
         assert lib.pgqa_status_string(code)
 
@@ -82,7 +82,7 @@ def test_plan_config_layout():
     PC = binding.PlanConfig
     assert PC.max_q_rows.offset == 24 and PC.decode_ctas.offset == 56
     assert PC.rope_max_position.offset == 60 and PC.rope_theta.offset == 64
-    assert ctypes.sizeof(PC) == 72
+    assert PC.prefill_kernel.offset == 72 and ctypes.sizeof(PC) == 80
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -114,7 +114,8 @@ def test_explicit_scale():
                           (3, 64, 128, "fp16"), (5, 128, 16, "bf16"), (16, 64, 64, "bf16"),
                           (12, 128, 16, "fp16")])
 @pytest.mark.parametrize("causal", [True, False])
-def test_prefill_segments(group, head_dim, page_size, dtype, causal):
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+def test_prefill_segments(group, head_dim, page_size, dtype, causal, prefill_kernel):
     """Chunks of query rows (tensor-core prefill tiles) mixed with decode rows,
     chunk lengths not multiples of 64 / G, plus a chunk longer than its history
     (its first rows have no admissible key under the causal mask)."""
@@ -124,6 +125,6 @@ def test_prefill_segments(group, head_dim, page_size, dtype, causal):
     w = W.custom("pf", lens, page_size, group * hkv, hkv, head_dim, dtype, 128, seed=group + head_dim,
                  qo_lens=qo, causal=causal)
     ro, rl = H.oracle_outputs(w)
-    out, lse, info = H.gpu_outputs(w)
+    out, lse, info = H.gpu_outputs(w, prefill_kernel=prefill_kernel)
     assert info["num_prefill_tiles"] > 0
-    H.compare(out, lse, ro, rl, f"prefill g{group} d{head_dim} ps{page_size} {dtype} causal={causal}")
+    H.compare(out, lse, ro, rl, f"prefill/{prefill_kernel} g{group} d{head_dim} ps{page_size} {dtype} causal={causal}")
