@@ -267,7 +267,8 @@ def run_ours(args, rank, world, local):
                    max_q_rows=w.rows, max_splits=args.max_splits, split_tokens=args.split_tokens,
                    ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel,
                    pipeline_stages=args.stages, decode_ctas=args.decode_ctas,
-                   rope_theta=args.rope_theta, rope_max_position=int(w.kv_lens.max()) if args.rope_theta > 0 else 0)
+                   rope_theta=args.rope_theta, rope_max_position=int(w.kv_lens.max()) if args.rope_theta > 0 else 0,
+                   prefill_kernel=args.prefill_kernel, prefill_splits=args.prefill_splits)
     stream = torch.cuda.Stream(device)
     positions = (torch.from_numpy(W.row_positions(w)).to(device)
                  if args.rope_theta > 0 and L["slots"] is not None else None)
@@ -384,6 +385,7 @@ def run_ours(args, rank, world, local):
     achieved = launch_bytes / per_launch_s / 1e9
     # the committed counters describe the default launch of this workload only
     default_launch = (args.decode_kernel != "cuda_core" and not args.rope_theta and not args.split_tokens and
+                      args.prefill_kernel == "auto" and not args.prefill_splits and
                       not args.max_splits and not args.stages and not args.decode_ctas and not args.ctas_per_sm)
     traffic = profiled_traffic(args.workload) if default_launch else None
     e2e_value = sum_over_ranks(b["per_step"] * args.steps, world, device) / t_e2e / 1e9
@@ -411,6 +413,7 @@ def run_ours(args, rank, world, local):
             "graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single",
             "decode_kernel": args.decode_kernel, "append_mode": args.append_mode if L["slots"] is not None else None,
             "rope_theta": args.rope_theta if args.rope_theta > 0 else None,
+            "prefill_kernel": args.prefill_kernel if w.qo_indptr is not None else None,
             "plan": {k: info[k] for k in ("num_items", "num_merge_tasks", "split_tokens", "max_splits_used",
                                           "num_sms")},
         },
@@ -544,6 +547,8 @@ def main(argv=None):
                     help="0: one CTA per work item; n: n persistent CTAs; -1: one persistent CTA per SM")
     ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
+    ap.add_argument("--prefill-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto")
+    ap.add_argument("--prefill-splits", type=int, default=0, help="key slices per prefill tile (0: automatic)")
     ap.add_argument("--rope-theta", type=float, default=0.0,
                     help="> 0: rotary embedding of q and the appended K rows with this base")
     ap.add_argument("--no-cpu-baseline", action="store_true")

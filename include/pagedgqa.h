@@ -137,9 +137,10 @@ typedef struct pgqa_plan_config {
     int rope_max_position; /* RoPE plans: positions 0 .. rope_max_position - 1 are valid */
     double rope_theta;    /* > 0: rotary position embedding with this base (see below);
                              0: none */
-    int prefill_kernel;   /* requests with several query rows: PGQA_PREFILL_AUTO (the
-                             tcgen05 kernel), PGQA_PREFILL_TCGEN05 or PGQA_PREFILL_MMA_SYNC
-                             (kept as a measured alternative) */
+    int prefill_kernel;   /* requests with several query rows: PGQA_PREFILL_TCGEN05 (5th-
+                             generation tensor cores, S and O in tensor memory) or
+                             PGQA_PREFILL_MMA_SYNC; PGQA_PREFILL_AUTO takes the mma.sync
+                             kernel, the faster one beside a ragged call's decode rows */
 } pgqa_plan_config;
 
 #define PGQA_PREFILL_AUTO 0

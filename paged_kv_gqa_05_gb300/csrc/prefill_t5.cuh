@@ -12,13 +12,17 @@
 // tile serves the whole group.  The 128 pairs are the M = 128 rows of the products,
 // one TMEM lane each.  Per 64-key tile:
 //   S[128 x 64]  = Q[128 x d] . K^T   tcgen05.mma, Q and K K-major in 128B-swizzled smem
-//   each thread loads its pair's row of S from TMEM (tcgen05.ld), applies the causal
-//   bound and the online softmax on its own row (no cross-lane reductions), and writes
-//   P back over S as two 16-bit terms (P = P_hi + P_lo);
+//   two threads per pair (warps w and w + 4 reach the same TMEM lanes) each load 32
+//   of the row's scores (tcgen05.ld), apply the causal bound and the online softmax
+//   (the row maximum is the one value they exchange, through shared memory; each keeps
+//   its own partial row sum), and write their P back over S as two 16-bit terms
+//   (P = P_hi + P_lo);
 //   O_t[128 x d] = P_hi . V + P_lo . V   tcgen05.mma with A from TMEM, V MN-major
-//   each thread folds its row of O_t into its fp32 output registers.
+//   each thread folds its d/2 columns of the row of O_t into fp32 output registers.
 // One thread issues the products and the TMA loads; completion is signalled through
-// mbarriers (tcgen05.commit); every wait is bounded.
+// mbarriers (tcgen05.commit); every wait is bounded.  The products run behind the
+// threads' work: while the threads take tile k's softmax, S for tile k is ready
+// (issued one tile earlier) and P.V of tile k-1 runs; its O_t is folded in after.
 #pragma once
 
 #include <climits>
@@ -32,6 +36,8 @@ template <int D>
 struct T5Cfg {
     static constexpr int KT = 64;                        // keys per tile
     static constexpr int MP = 128;                       // pairs per CTA (TMEM lanes, MMA M)
+    static constexpr int NT = 256;                       // threads: two per pair
+    static constexpr int DH = D / 2;                     // output columns per thread
     static constexpr int ST = D == 64 ? 4 : 2;           // K/V stages: two CTAs per SM either way
     static constexpr int HALVES = D / 64;
     static constexpr int HALF_BYTES = KT * 128;          // 64 keys x 64 channels of K or V
@@ -40,13 +46,17 @@ struct T5Cfg {
     static constexpr int QHALF_BYTES = MP * 128;         // 128 pairs x 64 channels of Q
     static constexpr int Q_BYTES = HALVES * QHALF_BYTES;
     static constexpr int PIPE_OFF = Q_BYTES;
-    static constexpr int BAR_OFF = PIPE_OFF + ST * STAGE_BYTES;  // ST stage barriers, then S, O
-    static constexpr int SLOT_OFF = BAR_OFF + (ST + 2) * 8;
+    static constexpr int BAR_OFF = PIPE_OFF + ST * STAGE_BYTES;  // ST stage barriers, then S[2], O[2]
+    static constexpr int SLOT_OFF = BAR_OFF + (ST + 4) * 8;
     static constexpr int PAGE_OFF = (SLOT_OFF + 4 + 15) / 16 * 16;
-    static constexpr int SMEM_BYTES = PAGE_OFF + kSlicePageCap * 4;
-    static constexpr uint32_t TMEM_COLS = 256;           // S / P: columns [0, 64); O_t: [64, 64 + D)
-    static constexpr int S_COL = 0, O_COL = 64;
-    static_assert(O_COL + D <= static_cast<int>(TMEM_COLS), "TMEM columns");
+    static constexpr int XCH_OFF = PAGE_OFF + kSlicePageCap * 4;   // [2][MP] floats exchanged per row
+    static constexpr int SMEM_BYTES = XCH_OFF + 2 * MP * 4;
+    // TMEM: two S / P buffers of 64 columns, then OBUF buffers of D columns for O_t, so the
+    // products of one tile run while the threads work on another
+    static constexpr int OBUF = D == 64 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr int S_COL = 0, O_COL = 128;
+    static_assert(O_COL + OBUF * D <= static_cast<int>(TMEM_COLS), "TMEM columns");
     static_assert(Q_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 };
 
@@ -57,7 +67,7 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c, int half_bytes) {
 }
 
 template <int D, bool ROPE, typename T>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     prefill_t5_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const PrefillParams p, int G) {
     using C = T5Cfg<D>;
@@ -65,13 +75,17 @@ __global__ void __launch_bounds__(128, 2)
     constexpr int CH = D / 8;
     extern __shared__ __align__(1024) uint8_t smem[];
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;  // TMEM lanes [32 quarter, +32): this warp's pairs
+    const int half = warp >> 2;    // which 32 keys of each tile and which d/2 output columns
+    const int prow = quarter * 32 + lane;  // the pair within the CTA (TMEM lane)
     uint8_t *qs = smem;
     uint8_t *pipe = smem + C::PIPE_OFF;
     const uint32_t bar0 = smem_addr(smem + C::BAR_OFF);
-    const uint32_t bar_s = bar0 + 8 * C::ST, bar_o = bar_s + 8;
+    const uint32_t bar_s = bar0 + 8 * C::ST, bar_o = bar_s + 16;  // two of each
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::SLOT_OFF);
     int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PAGE_OFF);
+    float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);
 
     if (smem_addr(smem) & 1023u) {  // the swizzled tiles assume this alignment of the window
         if (tid == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
@@ -83,7 +97,7 @@ __global__ void __launch_bounds__(128, 2)
     const bool fused = p.k_new != nullptr;
     const int new_begin = it.n_keys - it.rows;  // the chunk's own keys (a fused call supplies them)
     // this thread's pair (row of every product)
-    const int pm = it.pair0 + tid;
+    const int pm = it.pair0 + prow;
     const int qi = pm / G, qh = pm - (pm / G) * G;
     const bool valid = qi < it.rows;
     int limit = !valid ? -1 : (p.causal ? it.n_keys - it.rows + qi : it.n_keys - 1);
@@ -103,7 +117,7 @@ __global__ void __launch_bounds__(128, 2)
     };
 
     if (tid == 0) {
-        for (int s = 0; s < C::ST + 2; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s < C::ST + 4; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_barrier_init();
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
@@ -114,8 +128,9 @@ __global__ void __launch_bounds__(128, 2)
     __syncthreads();
     t5::fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + C::S_COL, t_o = tmem + C::O_COL;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    auto t_s = [&](int kt) { return tmem + C::S_COL + 64u * static_cast<uint32_t>(kt & 1); };
+    auto t_o = [&](int kt) { return tmem + C::O_COL + static_cast<uint32_t>(D * (kt % C::OBUF)); };
     const uint64_t policy = l2_evict_first_policy();
 
     auto issue = [&](int kt) {
@@ -156,64 +171,68 @@ __global__ void __launch_bounds__(128, 2)
     if (!p.prefetch_pool && tid == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
 
-    // ---- Q: this thread's pair row into the swizzled K-major tile (zeros for no pair)
+    // ---- Q: the pair rows into the swizzled K-major tile (zeros for no pair).  Each of the
+    // two threads of a pair takes chunks c and c + CH/2 (rotate-half partners) for its
+    // quarter of c in [0, CH/2).
     {
-        uint4 v[CH];
+        constexpr int CQ = CH / 4;  // first-half chunks per thread
         const T *qrow = static_cast<const T *>(p.q) +
                         (static_cast<size_t>(it.q_row0 + (valid ? qi : 0)) * p.num_qo_heads + it.kv_head * G +
                          (valid ? qh : 0)) * D;
 #pragma unroll
-        for (int c = 0; c < CH; ++c)
-            v[c] = valid ? __ldg(reinterpret_cast<const uint4 *>(qrow + c * 8)) : make_uint4(0u, 0u, 0u, 0u);
-        if (ROPE && valid) {
-            // rotate-half pairs: chunk c of the first half with chunk c + CH/2
-            const float2 *cs = p.rope_cs + static_cast<size_t>(new_begin + qi) * (D / 2);
-#pragma unroll
-            for (int c = 0; c < CH / 2; ++c) {
-                uint32_t lo[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-                uint32_t hi[4] = {v[c + CH / 2].x, v[c + CH / 2].y, v[c + CH / 2].z, v[c + CH / 2].w};
+        for (int u = 0; u < CQ; ++u) {
+            const int c = half * CQ + u;
+            uint4 lo4 = valid ? __ldg(reinterpret_cast<const uint4 *>(qrow + c * 8)) : make_uint4(0u, 0u, 0u, 0u);
+            uint4 hi4 =
+                valid ? __ldg(reinterpret_cast<const uint4 *>(qrow + (c + CH / 2) * 8)) : make_uint4(0u, 0u, 0u, 0u);
+            if (ROPE && valid) {
+                const float2 *cs = p.rope_cs + static_cast<size_t>(new_begin + qi) * (D / 2);
+                uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     rope_rotate2<T>(lo[j], hi[j], __ldg(reinterpret_cast<const float4 *>(cs + 8 * c + 2 * j)));
-                v[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                v[c + CH / 2] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                lo4 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                hi4 = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             }
+            *reinterpret_cast<uint4 *>(qs + swz_off(prow, c, C::QHALF_BYTES)) = lo4;
+            *reinterpret_cast<uint4 *>(qs + swz_off(prow, c + CH / 2, C::QHALF_BYTES)) = hi4;
         }
-#pragma unroll
-        for (int c = 0; c < CH; ++c) *reinterpret_cast<uint4 *>(qs + swz_off(tid, c, C::QHALF_BYTES)) = v[c];
     }
     fence_proxy_async_smem();  // generic stores before the products read the tile
     __syncthreads();
 
-    float o[D];
+    float o[C::DH];  // output columns [DH half, DH half + DH) of this pair's row
 #pragma unroll
-    for (int j = 0; j < D; ++j) o[j] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;  // running max (scaled log2 units) and sum of this row
+    for (int j = 0; j < C::DH; ++j) o[j] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // running row max (scaled log2 units); this thread's partial sum
     constexpr uint32_t id_s = t5::idesc_f16<T>(C::MP, C::KT, false);
     constexpr uint32_t id_o = t5::idesc_f16<T>(C::MP, D, true);
     constexpr uint64_t kmaj = t5::smem_desc_bits(16, 1024);
     constexpr uint64_t vmaj = t5::smem_desc_bits(C::HALF_BYTES, 1024);
 
+    // ---- the pipeline.  Counters are CTA-uniform: every decision below is.
     bool ok = true;
-    int waited = 0;
-    for (int kt = 0; kt < ntiles; ++kt) {
+    int tma_issued = pre, tma_waited = 0;   // TMA tiles [0, tma_issued) requested, [0, tma_waited) landed
+    int s_issued = -1, s_waited = -1;       // S products issued / waited for
+    int pv_issued = -1, pv_waited = -1;     // P.V products issued / waited for
+
+    // Tile kt's stage has landed; the chunk's own new rows (fused append) and zeros over V
+    // rows past the slice end (P is 0 there, but 0 x NaN would not be) go in with generic
+    // stores before the products read it.
+    auto prepare = [&](int kt) -> bool {
         const int s = kt % C::ST;
         if (!__syncthreads_and(mbar_wait_bounded(bar0 + 8 * s, (kt / C::ST) & 1))) {
             if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            ok = false;
-            break;
+            return false;
         }
-        waited = kt + 1;
+        tma_waited = kt + 1;
         uint8_t *kp = pipe + s * C::STAGE_BYTES;
         uint8_t *vp = kp + C::TILE_BYTES;
         const int t0 = key_begin + kt * C::KT;
         const int nvalid = min(C::KT, key_end - t0);
-
-        // ---- generic stores into the stage: the chunk's own new rows (fused append), and
-        // zeros over V rows past the slice end (P is 0 there, but 0 x NaN would not be)
         bool wrote = false;
         if (fused && max(new_begin, t0) < t0 + nvalid) {
-            for (int idx = tid; idx < nvalid * 2 * CH; idx += 128) {
+            for (int idx = tid; idx < nvalid * 2 * CH; idx += C::NT) {
                 const int r = idx / (2 * CH);
                 const int rem = idx - r * 2 * CH;
                 const bool isv = rem >= CH;
@@ -225,7 +244,7 @@ __global__ void __launch_bounds__(128, 2)
             wrote = true;
         }
         if (nvalid < C::KT) {
-            for (int idx = tid; idx < (C::KT - nvalid) * CH; idx += 128) {
+            for (int idx = tid; idx < (C::KT - nvalid) * CH; idx += C::NT) {
                 const int r = nvalid + idx / CH, ch = idx - (idx / CH) * CH;
                 *reinterpret_cast<uint4 *>(vp + swz_off(r, ch, C::HALF_BYTES)) = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -235,56 +254,102 @@ __global__ void __launch_bounds__(128, 2)
             fence_proxy_async_smem();
             __syncthreads();
         }
-
-        // ---- S = Q . K^T into TMEM
+        return true;
+    };
+    // S = Q . K^T of tile kt into S buffer kt & 1 (one thread)
+    auto issue_s = [&](int kt) {
         if (tid == 0) {
+            const uint32_t kb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES);
             t5::fence_after();
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
                 const uint32_t kofs = (ks >> 2) * C::HALF_BYTES + (ks & 3) * 32;
                 const uint32_t qofs = (ks >> 2) * C::QHALF_BYTES + (ks & 3) * 32;
-                t5::mma_ss(t_s, t5::smem_desc(smem_addr(qs) + qofs, kmaj), t5::smem_desc(smem_addr(kp) + kofs, kmaj),
-                           id_s, ks > 0);
+                t5::mma_ss(t_s(kt), t5::smem_desc(smem_addr(qs) + qofs, kmaj), t5::smem_desc(kb + kofs, kmaj), id_s,
+                           ks > 0);
             }
-            t5::commit(bar_s);
+            t5::commit(bar_s + 8 * (kt & 1));
         }
-        if (!__syncthreads_and(mbar_wait_bounded(bar_s, kt & 1))) {
+        s_issued = kt;
+    };
+    // O_t = P_hi . V + P_lo . V of tile kt into O buffer kt % OBUF (one thread)
+    auto issue_pv = [&](int kt) {
+        if (tid == 0) {
+            const uint32_t vb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES);
+            t5::fence_after();
+#pragma unroll
+            for (int kk = 0; kk < C::KT / 16; ++kk)
+                t5::mma_ts(t_o(kt), t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < C::KT / 16; ++kk)
+                t5::mma_ts(t_o(kt), t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
+            t5::commit(bar_o + 8 * (kt % C::OBUF));
+        }
+        pv_issued = kt;
+    };
+    // o = o * a + O_t of tile kt (every thread, its own row); false when the wait gave up
+    auto fold = [&](int kt, float a) -> bool {
+        const bool got = mbar_wait_bounded(bar_o + 8 * (kt % C::OBUF), (kt / C::OBUF) & 1);
+        pv_waited = kt;
+        if (!got) return false;
+        t5::fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < C::DH; c0 += 32) {
+            uint32_t r[32];
+            t5::ld32(t_o(kt) + lane_base + C::DH * half + c0, r);
+            t5::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(o[c0 + j], a, __uint_as_float(r[j]));
+        }
+        return true;
+    };
+
+    if (ntiles > 0) {
+        ok = prepare(0);
+        if (ok) issue_s(0);
+    }
+    float prev_alpha = 1.f;
+    for (int kt = 0; ok && kt < ntiles; ++kt) {
+        // ---- 1. S of tile kt: mask, online softmax, P (two 16-bit terms) back over S
+        if (!__syncthreads_and(mbar_wait_bounded(bar_s + 8 * (kt & 1), (kt >> 1) & 1))) {
             if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
             ok = false;
             break;
         }
+        s_waited = kt;
         t5::fence_after();
-
-        // ---- this row's scores: mask, online softmax, P (two 16-bit terms) back into TMEM
-        float sc[C::KT];
+        const int t0 = key_begin + kt * C::KT;
+        const int k0 = t0 + 32 * half;  // this thread's 32 keys
+        float sc[32];
         {
-            uint32_t r0[32], r1[32];
-            t5::ld32(t_s + lane_base, r0);
-            t5::ld32(t_s + lane_base + 32, r1);
+            uint32_t r0[32];
+            t5::ld32(t_s(kt) + lane_base + 32 * half, r0);
             t5::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                sc[j] = __uint_as_float(r0[j]);
-                sc[32 + j] = __uint_as_float(r1[j]);
-            }
+            for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r0[j]);
         }
-        if (t0 + C::KT - 1 > limit) {
+        if (k0 + 31 > limit) {
 #pragma unroll
-            for (int j = 0; j < C::KT; ++j)
-                if (t0 + j > limit) sc[j] = -INFINITY;
+            for (int j = 0; j < 32; ++j)
+                if (k0 + j > limit) sc[j] = -INFINITY;
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < C::KT; ++j) mx = fmaxf(mx, sc[j]);
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sc[j]);
+        // the row max over both halves (the buffer's previous values were read before the
+        // barrier that ended the last tile)
+        xch[half * C::MP + prow] = mx;
+        __syncthreads();
+        mx = fmaxf(mx, xch[(1 - half) * C::MP + prow]);
         const float mn = fmaxf(m_run, mx * p.scale_log2);  // the scale is positive
         const float alpha = (mn == m_run) ? 1.f : ex2_approx(m_run - mn);
         m_run = mn;
         const float neg_m = (mn == -INFINITY) ? 0.f : -mn;  // a row with no key yet: every P is 0
         {
-            uint32_t ph[32], pl[32];
+            uint32_t ph[16], pl[16];
             float lsum = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
                 const float p0 = ex2_approx(fmaf(sc[2 * j], p.scale_log2, neg_m));
                 const float p1 = ex2_approx(fmaf(sc[2 * j + 1], p.scale_log2, neg_m));
                 lsum += p0 + p1;
@@ -293,49 +358,57 @@ __global__ void __launch_bounds__(128, 2)
                 pl[j] = M::pack(p0 - f.x, p1 - f.y);
             }
             l_run = l_run * alpha + lsum;
-            t5::st32(t_s + lane_base, ph);       // P_hi: columns [0, 32)
-            t5::st32(t_s + lane_base + 32, pl);  // P_lo: columns [32, 64)
+            // keys [32 half, +32) are columns [16 half, +16) of P_hi ([0, 32)) and of P_lo ([32, 64))
+            t5::st16(t_s(kt) + lane_base + 16 * half, ph);
+            t5::st16(t_s(kt) + lane_base + 32 + 16 * half, pl);
             t5::wait_st();
         }
-        t5::fence_before();
-        __syncthreads();
-
-        // ---- O_t = P_hi . V + P_lo . V into TMEM
-        if (tid == 0) {
-            t5::fence_after();
-#pragma unroll
-            for (int kk = 0; kk < C::KT / 16; ++kk)
-                t5::mma_ts(t_o, t_s + 8 * kk, t5::smem_desc(smem_addr(vp) + kk * 2048, vmaj), id_o, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < C::KT / 16; ++kk)
-                t5::mma_ts(t_o, t_s + 32 + 8 * kk, t5::smem_desc(smem_addr(vp) + kk * 2048, vmaj), id_o, true);
-            t5::commit(bar_o);
+        // ---- 2. O_t of tile kt - 1 (its product ran during this softmax); its stage is free
+        bool folded = true;
+        if (kt >= 1) {
+            folded = fold(kt - 1, prev_alpha);
+            if (kt - 1 + C::ST < ntiles) {
+                if (tid == 0) issue(kt - 1 + C::ST);
+                tma_issued = kt - 1 + C::ST + 1;
+            }
         }
-        if (!__syncthreads_and(mbar_wait_bounded(bar_o, kt & 1))) {
+        prev_alpha = alpha;
+        // ---- 3. every thread's P_kt is in TMEM and its reads of O_t are done
+        t5::fence_before();
+        if (!__syncthreads_and(folded)) {
             if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
             ok = false;
             break;
         }
-        t5::fence_after();
-        // both products have read the stage: it can be refilled while this row folds O_t in
-        if (tid == 0 && kt + C::ST < ntiles) issue(kt + C::ST);
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            t5::ld32(t_o + lane_base + c0, r);
-            t5::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(o[c0 + j], alpha, __uint_as_float(r[j]));
+        // ---- 4. P.V of tile kt
+        issue_pv(kt);
+        // ---- 5. S of tile kt + 1 (its buffer's P was read by the product waited for in 2)
+        if (kt + 1 < ntiles) {
+            if (!prepare(kt + 1)) {
+                ok = false;
+                break;
+            }
+            issue_s(kt + 1);
         }
     }
-    if (!ok && tid == 0) {
-        const int issued = ntiles < waited + C::ST ? ntiles : waited + C::ST;
-        for (int kt = waited; kt < issued; ++kt) mbar_wait_bounded(bar0 + 8 * (kt % C::ST), (kt / C::ST) & 1);
+    if (ok && ntiles > 0) {
+        if (!fold(ntiles - 1, prev_alpha)) {
+            if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+            ok = false;
+        }
+    }
+    if (!ok) {  // drain what is still in flight (bounded) before TMEM and smem go away
+        if (pv_issued > pv_waited)
+            mbar_wait_bounded(bar_o + 8 * (pv_issued % C::OBUF), (pv_issued / C::OBUF) & 1);
+        if (s_issued > s_waited) mbar_wait_bounded(bar_s + 8 * (s_issued & 1), (s_issued >> 1) & 1);
+        if (tid == 0)
+            for (int kt = tma_waited; kt < tma_issued; ++kt)
+                mbar_wait_bounded(bar0 + 8 * (kt % C::ST), (kt / C::ST) & 1);
     }
 
     // ---- fused append: the split-0 CTA holding pair (i, head 0) stores row i's new K/V
     if (fused && it.split == 0) {
-        for (int idx = tid; idx < C::MP * 2 * CH; idx += 128) {
+        for (int idx = tid; idx < C::MP * 2 * CH; idx += C::NT) {
             const int mloc = idx / (2 * CH);
             const int m = it.pair0 + mloc;
             if (m % G != 0) continue;
@@ -364,33 +437,37 @@ __global__ void __launch_bounds__(128, 2)
         t5::dealloc(tmem, C::TMEM_COLS);
     }
 
-    // ---- normalise and store this thread's row
+    // ---- normalise and store this thread's columns of its pair's row
+    xch[half * C::MP + prow] = l_run;  // the row sum is the sum of both threads' parts
+    __syncthreads();
     if (!valid) return;
-    const float L = l_run;
+    const float L = l_run + xch[(1 - half) * C::MP + prow];
     // L == 0 only for a row with no admissible key; NaN (a poisoned row) propagates.
     const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
     const float lse2 = (L == 0.f) ? -INFINITY : m_run + lg2_approx(L);
     if (it.part_base >= 0) {  // split keys: normalised partial + its log2-sum-exp
         const size_t slot = static_cast<size_t>(it.part_base + qi * it.num_splits + it.split) * G + qh;
-        float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D);
+        float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D + C::DH * half);
 #pragma unroll
-        for (int j = 0; j < D; j += 4) dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
-        p.partial_lse[slot] = lse2;
+        for (int j = 0; j < C::DH; j += 4)
+            dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+        if (half == 0) p.partial_lse[slot] = lse2;
         return;
     }
     const size_t row = static_cast<size_t>(it.q_row0 + qi) * p.num_qo_heads + it.kv_head * G + qh;
     if (p.out_dtype == PGQA_FP32) {
-        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * D);
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * D + C::DH * half);
 #pragma unroll
-        for (int j = 0; j < D; j += 4) dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
+        for (int j = 0; j < C::DH; j += 4)
+            dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
     } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + row * D);
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + row * D + C::DH * half);
 #pragma unroll
-        for (int j = 0; j < D; j += 8)
+        for (int j = 0; j < C::DH; j += 8)
             dst[j / 8] = make_uint4(M::pack(o[j] * inv, o[j + 1] * inv), M::pack(o[j + 2] * inv, o[j + 3] * inv),
                                     M::pack(o[j + 4] * inv, o[j + 5] * inv), M::pack(o[j + 6] * inv, o[j + 7] * inv));
     }
-    if (p.lse != nullptr) p.lse[row] = lse2 * 0.6931471805599453f;
+    if (half == 0 && p.lse != nullptr) p.lse[row] = lse2 * 0.6931471805599453f;
 }
 
 template <int D, bool ROPE, typename T>
@@ -410,7 +487,7 @@ cudaError_t launch_prefill_t5_r(int group, const CUtensorMap &tm_k, const CUtens
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(C::NT);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

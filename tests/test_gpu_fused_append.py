@@ -61,14 +61,15 @@ def test_fused_shapes(head_dim, page_size, dtype, heads):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_fused_multi_row(causal):
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+def test_fused_multi_row(causal, prefill_kernel):
     """A chunk of L query rows per request appends L rows (the ragged step)."""
     w = W.custom("fzr", [40, 7, 300, 64], 16, 14, 2, 64, "bf16", 64, seed=11, qo_lens=[13, 1, 5, 64],
                  causal=causal)
     H.new_rows_for_query_rows(w)
     ro, rl = H.oracle_outputs(w)
-    out, lse, dev, _ = fused_gpu(w, split_tokens=64)
-    H.compare(out, lse, ro, rl, f"fused multi-row causal={causal}")
+    out, lse, dev, _ = fused_gpu(w, split_tokens=64, prefill_kernel=prefill_kernel)
+    H.compare(out, lse, ro, rl, f"fused multi-row causal={causal} {prefill_kernel}")
     check_pool(w, dev)
 
 

@@ -128,14 +128,16 @@ def test_rope_shapes(head_dim, page_size, dtype, hq, hkv):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("head_dim,group", [(64, 7), (128, 6), (128, 16)])
-def test_rope_prefill_segments(causal, head_dim, group):
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+def test_rope_prefill_segments(causal, head_dim, group, prefill_kernel):
     """Multi-row requests (prefill tiles): each query row and each new K row turns at its
     own position."""
     lens, qo = [300, 5, 1030, 77, 3], [70, 1, 200, 77, 3]
     w = W.custom("ropepf", lens, 64, group * 2, 2, head_dim, "bf16", 64, seed=group + head_dim,
                  qo_lens=qo, causal=causal)
     H.new_rows_for_query_rows(w)
-    check_fused(w, f"rope prefill g{group} d{head_dim} causal={causal}")
+    check_fused(w, f"rope prefill g{group} d{head_dim} causal={causal} {prefill_kernel}",
+                prefill_kernel=prefill_kernel)
 
 
 def test_two_step_equals_fused():
