@@ -222,6 +222,15 @@ def wide_group(seed: int = 0, batch: int = 64, cached: int = 2048, num_pages: in
                               f"Hq32/Hkv2/d128 (group 16), bf16, pool {num_pages} pages")
 
 
+def prefill_chunk(seed: int = 0, chunk: int = 512, cached: int = 1024, num_pages: int = 8192) -> Workload:
+    """The ragged workload's prompt chunk alone: one request of `chunk` causal query
+    rows over its cached + own keys."""
+    return custom(f"prefill_chunk_{chunk}x{cached + chunk}", [cached + chunk], 64, 14, 2, 64, "bf16", num_pages,
+                  seed=seed + 3, qo_lens=[chunk], causal=True,
+                  description=f"1 prefill segment of {chunk} rows over {cached}+{chunk} keys (causal), page 64, "
+                              f"Hq14/Hkv2/d64, bf16, pool {num_pages}")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "qwen05_decode": qwen05_decode,
@@ -230,6 +239,7 @@ WORKLOADS = {
     "long_context_b4": lambda seed=0: long_context(seed, batch=4),
     "ragged": ragged,
     "wide_group": wide_group,
+    "prefill_chunk": prefill_chunk,
 }
 
 
@@ -245,6 +255,18 @@ def row_positions(w: Workload) -> np.ndarray:
         r0, r1 = (b, b + 1) if w.qo_indptr is None else (int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
         pos[r0:r1] = int(w.kv_lens[b]) - (r1 - r0) + np.arange(r1 - r0)
     return pos
+
+
+def algorithmic_flops(w: Workload) -> int:
+    """Multiply-adds of the attention counted as 2 flops each: q.k and p.v over every
+    admissible (query row, head, key) triple, 4 d flops per triple."""
+    triples = 0
+    for b in range(w.batch):
+        r0, r1 = (b, b + 1) if w.qo_indptr is None else (int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
+        n, L = int(w.kv_lens[b]), r1 - r0
+        for i in range(L):
+            triples += max(0, min(n, n - L + i + 1)) if w.causal else n
+    return triples * w.num_qo_heads * 4 * w.head_dim
 
 
 def algorithmic_bytes(w: Workload, out_elem_bytes: int = 2) -> dict:
