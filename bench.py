@@ -88,11 +88,18 @@ KERNEL_SOURCES = ("paged_kv_gqa_05_gb300/csrc/decode_tc.cuh", "paged_kv_gqa_05_g
 
 
 def kernel_sources_hash() -> str:
+    """Hash of the decode kernel's sources: decode_tc.cuh and common.cuh without the block
+    of host-side launcher declarations (which does not change the compiled kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+            text = fh.read()
+        if f.endswith("common.cuh"):
+            text = re.sub(rb"// Launchers \(defined in the kernel translation units\)\..*?// Device helpers \(inline PTX\)",
+                          b"", text, flags=re.S)
+        h.update(text)
     return h.hexdigest()[:16]
 
 
