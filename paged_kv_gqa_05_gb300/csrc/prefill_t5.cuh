@@ -19,10 +19,21 @@
 //   (P = P_hi + P_lo);
 //   O_t[128 x d] = P_hi . V + P_lo . V   tcgen05.mma with A from TMEM, V MN-major
 //   each thread folds its d/2 columns of the row of O_t into fp32 output registers.
-// One thread issues the products and the TMA loads; completion is signalled through
-// mbarriers (tcgen05.commit); every wait is bounded.  The products run behind the
-// threads' work: while the threads take tile k's softmax, S for tile k is ready
-// (issued one tile earlier) and P.V of tile k-1 runs; its O_t is folded in after.
+//
+// Warp specialisation.  Issuing a product holds the issuing thread for about as long
+// as the tensor pipe takes to run it (measured on GB300: ~23 ns per 128x64x16 product,
+// ~37 ns with two CTAs per SM), so a ninth warp does nothing but wait for the K/V
+// copies, make the generic stores a stage needs (the chunk's own new rows, zeros past
+// the slice end) and issue the products; warps 0-7 do only the softmax and the folds.
+// They hand over through mbarriers:
+//   S ready (tcgen05.commit, one per S buffer) -> the softmax of tile k;
+//   P ready (256 arrivals, two barriers by tile parity): P of tile k is in TMEM and
+//     O_t of tile k-1 has been read -> the issue warp's P.V of tile k;
+//   P.V done (tcgen05.commit, two by parity) -> the folds, and the issue warp's reuse
+//     of the tile's stage and S buffer.
+// With three S buffers (d = 64) S runs two tiles ahead of P.V, so the threads find
+// each tile's scores ready.  Every wait is bounded; a thread whose wait gives up
+// reports it, stops waiting and still takes part in every barrier, so the CTA ends.
 #pragma once
 
 #include <climits>
@@ -36,9 +47,11 @@ template <int D>
 struct T5Cfg {
     static constexpr int KT = 64;                        // keys per tile
     static constexpr int MP = 128;                       // pairs per CTA (TMEM lanes, MMA M)
-    static constexpr int NT = 256;                       // threads: two per pair
+    static constexpr int NT = 256;                       // softmax threads (warps 0-7): two per pair
+    static constexpr int NTHREADS = NT + 32;             // + the issue warp
     static constexpr int DH = D / 2;                     // output columns per thread
-    static constexpr int ST = D == 64 ? 4 : 2;           // K/V stages: two CTAs per SM either way
+    static constexpr int ST = D == 64 ? 5 : 2;           // K/V stages: two CTAs per SM either way
+    static constexpr int NSB = D == 64 ? 3 : 2;          // S / P buffers in TMEM
     static constexpr int HALVES = D / 64;
     static constexpr int HALF_BYTES = KT * 128;          // 64 keys x 64 channels of K or V
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
@@ -46,17 +59,17 @@ struct T5Cfg {
     static constexpr int QHALF_BYTES = MP * 128;         // 128 pairs x 64 channels of Q
     static constexpr int Q_BYTES = HALVES * QHALF_BYTES;
     static constexpr int PIPE_OFF = Q_BYTES;
-    static constexpr int BAR_OFF = PIPE_OFF + ST * STAGE_BYTES;  // ST stage barriers, then S[2], O[2]
-    static constexpr int SLOT_OFF = BAR_OFF + (ST + 4) * 8;
+    static constexpr int BAR_OFF = PIPE_OFF + ST * STAGE_BYTES;
+    static constexpr int NBAR = ST + NSB + 2 + 2;        // stages, S buffers, P.V done [2], P ready [2]
+    static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
     static constexpr int PAGE_OFF = (SLOT_OFF + 4 + 15) / 16 * 16;
-    static constexpr int XCH_OFF = PAGE_OFF + kSlicePageCap * 4;   // [2][MP] floats exchanged per row
-    static constexpr int SMEM_BYTES = XCH_OFF + 2 * MP * 4;
-    // TMEM: two S / P buffers of 64 columns, then OBUF buffers of D columns for O_t, so the
-    // products of one tile run while the threads work on another
-    static constexpr int OBUF = D == 64 ? 2 : 1;
+    static constexpr int XCH_OFF = PAGE_OFF + kSlicePageCap * 4;  // [3][2][MP] floats: row max by tile parity, row sum
+    static constexpr int SMEM_BYTES = XCH_OFF + 3 * 2 * MP * 4;
+    // TMEM: NSB S / P buffers of 64 columns, then D columns for O_t; 256 columns leave
+    // room for two CTAs per SM.
     static constexpr uint32_t TMEM_COLS = 256;
-    static constexpr int S_COL = 0, O_COL = 128;
-    static_assert(O_COL + OBUF * D <= static_cast<int>(TMEM_COLS), "TMEM columns");
+    static constexpr int S_COL = 0, O_COL = 64 * NSB;
+    static_assert(O_COL + D <= static_cast<int>(TMEM_COLS), "TMEM columns");
     static_assert(Q_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 };
 
@@ -66,8 +79,10 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c, int half_bytes) {
     return (c >> 3) * half_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
+// Two CTAs per SM: 18 warps put five on some of the SM's four sub-partitions, whose
+// 16K registers then allow 96 a thread.
 template <int D, bool ROPE, typename T>
-__global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
+__global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     prefill_t5_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const PrefillParams p, int G) {
     using C = T5Cfg<D>;
@@ -76,13 +91,14 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;  // TMEM lanes [32 quarter, +32): this warp's pairs
-    const int half = warp >> 2;    // which 32 keys of each tile and which d/2 output columns
-    const int prow = quarter * 32 + lane;  // the pair within the CTA (TMEM lane)
+    const bool issuer = warp == C::NT / 32;  // the issue warp
+    const int quarter = warp & 3;            // TMEM lanes [32 quarter, +32): this warp's pairs
+    const int half = (warp >> 2) & 1;        // which 32 keys of each tile and which d/2 output columns
+    const int prow = quarter * 32 + lane;    // the pair within the CTA (TMEM lane)
     uint8_t *qs = smem;
     uint8_t *pipe = smem + C::PIPE_OFF;
     const uint32_t bar0 = smem_addr(smem + C::BAR_OFF);
-    const uint32_t bar_s = bar0 + 8 * C::ST, bar_o = bar_s + 16;  // two of each
+    const uint32_t bar_s = bar0 + 8 * C::ST, bar_o = bar_s + 8 * C::NSB, bar_p = bar_o + 16;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::SLOT_OFF);
     int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PAGE_OFF);
     float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);
@@ -96,10 +112,10 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     const int key_begin = it.key_begin, key_end = it.key_end;
     const bool fused = p.k_new != nullptr;
     const int new_begin = it.n_keys - it.rows;  // the chunk's own keys (a fused call supplies them)
-    // this thread's pair (row of every product)
+    // this thread's pair (row of every product); the issue warp computes one it never uses
     const int pm = it.pair0 + prow;
     const int qi = pm / G, qh = pm - (pm / G) * G;
-    const bool valid = qi < it.rows;
+    const bool valid = !issuer && qi < it.rows;
     int limit = !valid ? -1 : (p.causal ? it.n_keys - it.rows + qi : it.n_keys - 1);
     limit = min(limit, key_end - 1);  // keys of this CTA's slice only
     // key tiles up to the largest admissible key of the CTA's pairs (rows grow with m)
@@ -116,8 +132,8 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
         return __ldg(reinterpret_cast<const uint4 *>(row + ch * 8));
     };
 
-    if (tid == 0) {
-        for (int s = 0; s < C::ST + 4; ++s) mbar_init(bar0 + 8 * s, 1);
+    if (issuer && lane == 0) {
+        for (int b = 0; b < C::NBAR; ++b) mbar_init(bar0 + 8 * b, b >= C::ST + C::NSB + 2 ? C::NT : 1);
         fence_barrier_init();
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
@@ -129,10 +145,11 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     t5::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    auto t_s = [&](int kt) { return tmem + C::S_COL + 64u * static_cast<uint32_t>(kt & 1); };
-    auto t_o = [&](int kt) { return tmem + C::O_COL + static_cast<uint32_t>(D * (kt % C::OBUF)); };
+    auto t_s = [&](int kt) { return tmem + C::S_COL + 64u * static_cast<uint32_t>(kt % C::NSB); };
+    const uint32_t t_o = tmem + C::O_COL;
     const uint64_t policy = l2_evict_first_policy();
 
+    // TMA of tile kt's K and V into its stage (issue warp, lane 0)
     auto issue = [&](int kt) {
         const int s = kt % C::ST;
         const uint32_t kdst = smem_addr(pipe + s * C::STAGE_BYTES);
@@ -164,17 +181,17 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     };
 
     const int pre = ntiles < C::ST ? ntiles : C::ST;
-    if (p.prefetch_pool && tid == 0)
+    if (p.prefetch_pool && issuer && lane == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
     pdl_wait();
     pdl_launch_dependents();
-    if (!p.prefetch_pool && tid == 0)
+    if (!p.prefetch_pool && issuer && lane == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
 
     // ---- Q: the pair rows into the swizzled K-major tile (zeros for no pair).  Each of the
     // two threads of a pair takes chunks c and c + CH/2 (rotate-half partners) for its
     // quarter of c in [0, CH/2).
-    {
+    if (!issuer) {
         constexpr int CQ = CH / 4;  // first-half chunks per thread
         const T *qrow = static_cast<const T *>(p.q) +
                         (static_cast<size_t>(it.q_row0 + (valid ? qi : 0)) * p.num_qo_heads + it.kv_head * G +
@@ -205,210 +222,205 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
 #pragma unroll
     for (int j = 0; j < C::DH; ++j) o[j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // running row max (scaled log2 units); this thread's partial sum
-    constexpr uint32_t id_s = t5::idesc_f16<T>(C::MP, C::KT, false);
-    constexpr uint32_t id_o = t5::idesc_f16<T>(C::MP, D, true);
-    constexpr uint64_t kmaj = t5::smem_desc_bits(16, 1024);
-    constexpr uint64_t vmaj = t5::smem_desc_bits(C::HALF_BYTES, 1024);
 
-    // ---- the pipeline.  Counters are CTA-uniform: every decision below is.
-    bool ok = true;
-    int tma_issued = pre, tma_waited = 0;   // TMA tiles [0, tma_issued) requested, [0, tma_waited) landed
-    int s_issued = -1, s_waited = -1;       // S products issued / waited for
-    int pv_issued = -1, pv_waited = -1;     // P.V products issued / waited for
-
-    // Tile kt's stage has landed; the chunk's own new rows (fused append) and zeros over V
-    // rows past the slice end (P is 0 there, but 0 x NaN would not be) go in with generic
-    // stores before the products read it.
-    auto prepare = [&](int kt) -> bool {
-        const int s = kt % C::ST;
-        if (!__syncthreads_and(mbar_wait_bounded(bar0 + 8 * s, (kt / C::ST) & 1))) {
-            if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            return false;
-        }
-        tma_waited = kt + 1;
-        uint8_t *kp = pipe + s * C::STAGE_BYTES;
-        uint8_t *vp = kp + C::TILE_BYTES;
-        const int t0 = key_begin + kt * C::KT;
-        const int nvalid = min(C::KT, key_end - t0);
-        bool wrote = false;
-        if (fused && max(new_begin, t0) < t0 + nvalid) {
-            for (int idx = tid; idx < nvalid * 2 * CH; idx += C::NT) {
-                const int r = idx / (2 * CH);
-                const int rem = idx - r * 2 * CH;
-                const bool isv = rem >= CH;
-                const int ch = rem - (isv ? CH : 0);
-                const int pos = t0 + r;
-                if (pos < new_begin) continue;
-                *reinterpret_cast<uint4 *>((isv ? vp : kp) + swz_off(r, ch, C::HALF_BYTES)) = new_chunk(isv, pos, ch);
+    if (issuer) {
+        // ================= the issue warp =================
+        constexpr uint32_t id_s = t5::idesc_f16<T>(C::MP, C::KT, false);
+        constexpr uint32_t id_o = t5::idesc_f16<T>(C::MP, D, true);
+        constexpr uint64_t kmaj = t5::smem_desc_bits(16, 1024);
+        constexpr uint64_t vmaj = t5::smem_desc_bits(C::HALF_BYTES, 1024);
+        bool live = true;                       // false once one of its waits gave up
+        int tma_issued = pre, tma_waited = 0;   // tiles [0, tma_issued) requested, [0, tma_waited) landed
+        int s_issued = -1, pv_issued = -1;      // the last S and P.V committed
+        // a bounded wait by the whole warp; the outcome is warp-uniform
+        auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+            const bool got = __all_sync(0xffffffffu, live && mbar_wait_bounded(bar, parity));
+            if (!got && live && lane == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+            live = live && got;
+            return got;
+        };
+        // Tile kt's stage: wait for it, make its generic stores (the chunk's own new rows;
+        // zeros over V rows past the slice end, where P is 0 but 0 x NaN would not be),
+        // then S = Q . K^T into S buffer kt % NSB.
+        auto stage_s = [&](int kt) {
+            const int s = kt % C::ST;
+            if (!wait_all(bar0 + 8 * s, (kt / C::ST) & 1)) return;
+            tma_waited = kt + 1;
+            uint8_t *kp = pipe + s * C::STAGE_BYTES;
+            uint8_t *vp = kp + C::TILE_BYTES;
+            const int t0 = key_begin + kt * C::KT;
+            const int nvalid = min(C::KT, key_end - t0);
+            if (fused && max(new_begin, t0) < t0 + nvalid) {
+                const int first = max(new_begin, t0) - t0;  // first new row of the tile
+                const int n = (nvalid - first) * 2 * CH;
+                constexpr int U = 8;  // loads in flight per lane
+                for (int base = 0; base < n; base += 32 * U) {
+                    uint4 v[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int idx = base + u * 32 + lane;
+                        if (idx < n) {
+                            const int r = first + idx / (2 * CH), rem = idx % (2 * CH);
+                            v[u] = new_chunk(rem >= CH, t0 + r, rem % CH);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int idx = base + u * 32 + lane;
+                        if (idx < n) {
+                            const int r = first + idx / (2 * CH), rem = idx % (2 * CH);
+                            *reinterpret_cast<uint4 *>((rem >= CH ? vp : kp) + swz_off(r, rem % CH, C::HALF_BYTES)) =
+                                v[u];
+                        }
+                    }
+                }
             }
-            wrote = true;
-        }
-        if (nvalid < C::KT) {
-            for (int idx = tid; idx < (C::KT - nvalid) * CH; idx += C::NT) {
-                const int r = nvalid + idx / CH, ch = idx - (idx / CH) * CH;
+            for (int idx = lane; idx < (C::KT - nvalid) * CH; idx += 32) {
+                const int r = nvalid + idx / CH, ch = idx % CH;
                 *reinterpret_cast<uint4 *>(vp + swz_off(r, ch, C::HALF_BYTES)) = make_uint4(0u, 0u, 0u, 0u);
             }
-            wrote = true;
-        }
-        if (wrote) {  // CTA-uniform
             fence_proxy_async_smem();
-            __syncthreads();
-        }
-        return true;
-    };
-    // S = Q . K^T of tile kt into S buffer kt & 1 (one thread)
-    auto issue_s = [&](int kt) {
-        if (tid == 0) {
-            const uint32_t kb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES);
-            t5::fence_after();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t kb = smem_addr(kp);
+                t5::fence_after();
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t kofs = (ks >> 2) * C::HALF_BYTES + (ks & 3) * 32;
-                const uint32_t qofs = (ks >> 2) * C::QHALF_BYTES + (ks & 3) * 32;
-                t5::mma_ss(t_s(kt), t5::smem_desc(smem_addr(qs) + qofs, kmaj), t5::smem_desc(kb + kofs, kmaj), id_s,
-                           ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t kofs = (ks >> 2) * C::HALF_BYTES + (ks & 3) * 32;
+                    const uint32_t qofs = (ks >> 2) * C::QHALF_BYTES + (ks & 3) * 32;
+                    t5::mma_ss(t_s(kt), t5::smem_desc(smem_addr(qs) + qofs, kmaj), t5::smem_desc(kb + kofs, kmaj),
+                               id_s, ks > 0);
+                }
+                t5::commit(bar_s + 8 * (kt % C::NSB));
             }
-            t5::commit(bar_s + 8 * (kt & 1));
-        }
-        s_issued = kt;
-    };
-    // O_t = P_hi . V + P_lo . V of tile kt into O buffer kt % OBUF (one thread)
-    auto issue_pv = [&](int kt) {
-        if (tid == 0) {
-            const uint32_t vb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES);
-            t5::fence_after();
+            s_issued = kt;
+        };
+        if (ntiles > 0) stage_s(0);
+        if (C::NSB == 3 && ntiles > 1) stage_s(1);
+        for (int kt = 0; kt < ntiles; ++kt) {
+            // P of tile kt is in TMEM and every thread has read O_t of tile kt - 1
+            if (wait_all(bar_p + 8 * (kt & 1), (kt >> 1) & 1)) {
+                if (lane == 0) {
+                    const uint32_t vb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES);
+                    t5::fence_after();
 #pragma unroll
-            for (int kk = 0; kk < C::KT / 16; ++kk)
-                t5::mma_ts(t_o(kt), t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, kk > 0);
+                    for (int kk = 0; kk < C::KT / 16; ++kk)
+                        t5::mma_ts(t_o, t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < C::KT / 16; ++kk)
-                t5::mma_ts(t_o(kt), t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
-            t5::commit(bar_o + 8 * (kt % C::OBUF));
-        }
-        pv_issued = kt;
-    };
-    // o = o * a + O_t of tile kt (every thread, its own row); false when the wait gave up
-    auto fold = [&](int kt, float a) -> bool {
-        const bool got = mbar_wait_bounded(bar_o + 8 * (kt % C::OBUF), (kt / C::OBUF) & 1);
-        pv_waited = kt;
-        if (!got) return false;
-        t5::fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < C::DH; c0 += 32) {
-            uint32_t r[32];
-            t5::ld32(t_o(kt) + lane_base + C::DH * half + c0, r);
-            t5::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(o[c0 + j], a, __uint_as_float(r[j]));
-        }
-        return true;
-    };
-
-    if (ntiles > 0) {
-        ok = prepare(0);
-        if (ok) issue_s(0);
-    }
-    float prev_alpha = 1.f;
-    for (int kt = 0; ok && kt < ntiles; ++kt) {
-        // ---- 1. S of tile kt: mask, online softmax, P (two 16-bit terms) back over S
-        if (!__syncthreads_and(mbar_wait_bounded(bar_s + 8 * (kt & 1), (kt >> 1) & 1))) {
-            if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            ok = false;
-            break;
-        }
-        s_waited = kt;
-        t5::fence_after();
-        const int t0 = key_begin + kt * C::KT;
-        const int k0 = t0 + 32 * half;  // this thread's 32 keys
-        float sc[32];
-        {
-            uint32_t r0[32];
-            t5::ld32(t_s(kt) + lane_base + 32 * half, r0);
-            t5::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r0[j]);
-        }
-        if (k0 + 31 > limit) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (k0 + j > limit) sc[j] = -INFINITY;
-        }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sc[j]);
-        // the row max over both halves (the buffer's previous values were read before the
-        // barrier that ended the last tile)
-        xch[half * C::MP + prow] = mx;
-        __syncthreads();
-        mx = fmaxf(mx, xch[(1 - half) * C::MP + prow]);
-        const float mn = fmaxf(m_run, mx * p.scale_log2);  // the scale is positive
-        const float alpha = (mn == m_run) ? 1.f : ex2_approx(m_run - mn);
-        m_run = mn;
-        const float neg_m = (mn == -INFINITY) ? 0.f : -mn;  // a row with no key yet: every P is 0
-        {
-            uint32_t ph[16], pl[16];
-            float lsum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float p0 = ex2_approx(fmaf(sc[2 * j], p.scale_log2, neg_m));
-                const float p1 = ex2_approx(fmaf(sc[2 * j + 1], p.scale_log2, neg_m));
-                lsum += p0 + p1;
-                ph[j] = M::pack(p0, p1);
-                const float2 f = unpack2<T>(ph[j]);
-                pl[j] = M::pack(p0 - f.x, p1 - f.y);
+                    for (int kk = 0; kk < C::KT / 16; ++kk)
+                        t5::mma_ts(t_o, t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
+                    t5::commit(bar_o + 8 * (kt & 1));
+                }
+                pv_issued = kt;
             }
-            l_run = l_run * alpha + lsum;
-            // keys [32 half, +32) are columns [16 half, +16) of P_hi ([0, 32)) and of P_lo ([32, 64))
-            t5::st16(t_s(kt) + lane_base + 16 * half, ph);
-            t5::st16(t_s(kt) + lane_base + 32 + 16 * half, pl);
-            t5::wait_st();
-        }
-        // ---- 2. O_t of tile kt - 1 (its product ran during this softmax); its stage is free
-        bool folded = true;
-        if (kt >= 1) {
-            folded = fold(kt - 1, prev_alpha);
-            if (kt - 1 + C::ST < ntiles) {
-                if (tid == 0) issue(kt - 1 + C::ST);
+            // P.V of tile kt - 1 is done: its stage takes tile kt - 1 + ST, and its S buffer
+            // (the last reader of which it was) takes S of tile kt + NSB - 1
+            if (kt >= 1 && live && wait_all(bar_o + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1) &&
+                kt - 1 + C::ST < ntiles) {
+                if (lane == 0) issue(kt - 1 + C::ST);
                 tma_issued = kt - 1 + C::ST + 1;
             }
+            if (kt + C::NSB - 1 < ntiles && live) stage_s(kt + C::NSB - 1);
         }
-        prev_alpha = alpha;
-        // ---- 3. every thread's P_kt is in TMEM and its reads of O_t are done
-        t5::fence_before();
-        if (!__syncthreads_and(folded)) {
-            if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            ok = false;
-            break;
-        }
-        // ---- 4. P.V of tile kt
-        issue_pv(kt);
-        // ---- 5. S of tile kt + 1 (its buffer's P was read by the product waited for in 2)
-        if (kt + 1 < ntiles) {
-            if (!prepare(kt + 1)) {
-                ok = false;
-                break;
-            }
-            issue_s(kt + 1);
-        }
-    }
-    if (ok && ntiles > 0) {
-        if (!fold(ntiles - 1, prev_alpha)) {
-            if (tid == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            ok = false;
-        }
-    }
-    if (!ok) {  // drain what is still in flight (bounded) before TMEM and smem go away
-        if (pv_issued > pv_waited)
-            mbar_wait_bounded(bar_o + 8 * (pv_issued % C::OBUF), (pv_issued / C::OBUF) & 1);
-        if (s_issued > s_waited) mbar_wait_bounded(bar_s + 8 * (s_issued & 1), (s_issued >> 1) & 1);
-        if (tid == 0)
+        // drain what is still in flight (bounded; immediate when every wait succeeded): a
+        // commit arrives once every earlier product of its thread is done, and each barrier
+        // has at most one phase pending
+        if (lane == 0) {
+            if (pv_issued >= 0) mbar_wait_bounded(bar_o + 8 * (pv_issued & 1), (pv_issued >> 1) & 1);
+            if (s_issued >= 0) mbar_wait_bounded(bar_s + 8 * (s_issued % C::NSB), (s_issued / C::NSB) & 1);
             for (int kt = tma_waited; kt < tma_issued; ++kt)
                 mbar_wait_bounded(bar0 + 8 * (kt % C::ST), (kt / C::ST) & 1);
+        }
+    } else {
+        // ================= the softmax warps =================
+        bool live = true;  // false once one of this thread's waits gave up
+        // o = o * a + O_t of tile kt (its own row)
+        auto fold = [&](int kt, float a) {
+            const bool got = live && mbar_wait_bounded(bar_o + 8 * (kt & 1), (kt >> 1) & 1);
+            if (!got && live) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+            live = got;
+            t5::fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < C::DH; c0 += 32) {
+                uint32_t r[32];
+                t5::ld32(t_o + lane_base + C::DH * half + c0, r);
+                t5::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(o[c0 + j], a, __uint_as_float(r[j]));
+            }
+        };
+        float prev_alpha = 1.f;
+        for (int kt = 0; kt < ntiles; ++kt) {
+            // ---- S of tile kt: mask, online softmax, P (two 16-bit terms) back over S
+            const bool got = live && mbar_wait_bounded(bar_s + 8 * (kt % C::NSB), (kt / C::NSB) & 1);
+            if (!got && live) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+            live = got;
+            t5::fence_after();
+            const int t0 = key_begin + kt * C::KT;
+            const int k0 = t0 + 32 * half;  // this thread's 32 keys
+            float sc[32];
+            {
+                uint32_t r0[32];
+                t5::ld32(t_s(kt) + lane_base + 32 * half, r0);
+                t5::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r0[j]);
+            }
+            if (k0 + 31 > limit) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (k0 + j > limit) sc[j] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sc[j]);
+            // the row max over both halves: warps w and w + 4 hold the same pairs.  The slots
+            // alternate with the tile parity, so a slot is rewritten only after the partner
+            // has passed the next exchange, that is after it read the slot.
+            float *xc = xch + (kt & 1) * 2 * C::MP;
+            xc[half * C::MP + prow] = mx;
+            named_bar_sync_id(1 + quarter, 64);
+            mx = fmaxf(mx, xc[(1 - half) * C::MP + prow]);
+            const float mn = fmaxf(m_run, mx * p.scale_log2);  // the scale is positive
+            const float alpha = (mn == m_run) ? 1.f : ex2_approx(m_run - mn);
+            m_run = mn;
+            const float neg_m = (mn == -INFINITY) ? 0.f : -mn;  // a row with no key yet: every P is 0
+            {
+                uint32_t ph[16], pl[16];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_approx(fmaf(sc[2 * j], p.scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(sc[2 * j + 1], p.scale_log2, neg_m));
+                    lsum += p0 + p1;
+                    ph[j] = M::pack(p0, p1);
+                    const float2 f = unpack2<T>(ph[j]);
+                    pl[j] = M::pack(p0 - f.x, p1 - f.y);
+                }
+                l_run = l_run * alpha + lsum;
+                // keys [32 half, +32) are columns [16 half, +16) of P_hi ([0, 32)) and of P_lo ([32, 64))
+                t5::st16(t_s(kt) + lane_base + 16 * half, ph);
+                t5::st16(t_s(kt) + lane_base + 32 + 16 * half, pl);
+                t5::wait_st();
+            }
+            // ---- O_t of tile kt - 1 (its product ran during this softmax)
+            if (kt >= 1) fold(kt - 1, prev_alpha);
+            prev_alpha = alpha;
+            // ---- P of tile kt is in TMEM and O_t is read: the issue warp may go on
+            t5::fence_before();
+            t5::arrive(bar_p + 8 * (kt & 1));
+        }
+        if (ntiles > 0) fold(ntiles - 1, prev_alpha);
+        // the row sum is the sum of both threads' parts
+        float *xl = xch + 2 * 2 * C::MP;
+        xl[half * C::MP + prow] = l_run;
+        named_bar_sync_id(1 + quarter, 64);
+        l_run += xl[(1 - half) * C::MP + prow];
     }
 
     // ---- fused append: the split-0 CTA holding pair (i, head 0) stores row i's new K/V
     if (fused && it.split == 0) {
-        for (int idx = tid; idx < C::MP * 2 * CH; idx += C::NT) {
+        for (int idx = tid; idx < C::MP * 2 * CH; idx += C::NTHREADS) {
             const int mloc = idx / (2 * CH);
             const int m = it.pair0 + mloc;
             if (m % G != 0) continue;
@@ -429,7 +441,8 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
         }
     }
 
-    // ---- TMEM back before the stores (every product has completed: the last wait above)
+    // ---- TMEM back once every product has completed (the issue warp's drain) and every
+    // thread's reads are done
     t5::fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -438,10 +451,8 @@ __global__ void __launch_bounds__(T5Cfg<D>::NT, 2)
     }
 
     // ---- normalise and store this thread's columns of its pair's row
-    xch[half * C::MP + prow] = l_run;  // the row sum is the sum of both threads' parts
-    __syncthreads();
     if (!valid) return;
-    const float L = l_run + xch[(1 - half) * C::MP + prow];
+    const float L = l_run;
     // L == 0 only for a row with no admissible key; NaN (a poisoned row) propagates.
     const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
     const float lse2 = (L == 0.f) ? -INFINITY : m_run + lg2_approx(L);
@@ -487,7 +498,7 @@ cudaError_t launch_prefill_t5_r(int group, const CUtensorMap &tm_k, const CUtens
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
-    cfg.blockDim = dim3(C::NT);
+    cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

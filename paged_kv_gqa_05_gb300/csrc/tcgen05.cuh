@@ -90,6 +90,12 @@ __device__ __forceinline__ void commit(uint32_t bar_saddr) {
                  : "memory");
 }
 
+// One arrival of this thread on an mbarrier (release: its earlier writes, and with
+// fence_before its earlier tensor-memory accesses, are ordered before the phase completes).
+__device__ __forceinline__ void arrive(uint32_t bar_saddr) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_saddr) : "memory");
+}
+
 // 32 consecutive 32-bit columns of this thread's lane.
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
