@@ -388,10 +388,15 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->box_rows = std::min(c.page_size, p->tile);
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
     p->stages = c.pipeline_stages == 3 ? 3 : 2;
-    // AUTO takes the mma.sync kernel: beside a ragged call's decode grid (the serving step) its
-    // smaller CTAs co-run better (512-row chunk + 127 decode rows: 44.7 us against 48.0 us),
-    // although alone on the GPU the tcgen05 kernel is faster (19.5 us against 25.9 us).
-    p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_TCGEN05 ? PGQA_PREFILL_TCGEN05 : PGQA_PREFILL_MMA_SYNC;
+    // AUTO takes the kernel measured faster on GB300 for 512-row causal chunks over 1536 keys:
+    // tcgen05 for d 64 (20.6 against 26.1 us; beside a ragged call's 127 decode rows the two
+    // tie) and for 16-head groups at d 128 (51.5 against 60.0 us); mma.sync for d 128 with
+    // groups of up to 8 (28.1 against 31.2 us), where 96 registers a thread make the
+    // tcgen05 kernel spill its 64-column output rows.
+    if (c.prefill_kernel == PGQA_PREFILL_AUTO)
+        p->prefill_kind = (c.head_dim == 64 || group > 8) ? PGQA_PREFILL_TCGEN05 : PGQA_PREFILL_MMA_SYNC;
+    else
+        p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_TCGEN05 ? PGQA_PREFILL_TCGEN05 : PGQA_PREFILL_MMA_SYNC;
     p->prefill_pairs = p->prefill_kind == PGQA_PREFILL_MMA_SYNC ? 64 : 128;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);

@@ -22,15 +22,17 @@
 //
 // Warp specialisation.  Issuing a product holds the issuing thread for about as long
 // as the tensor pipe takes to run it (measured on GB300: ~23 ns per 128x64x16 product,
-// ~37 ns with two CTAs per SM), so a ninth warp does nothing but wait for the K/V
-// copies, make the generic stores a stage needs (the chunk's own new rows, zeros past
-// the slice end) and issue the products; warps 0-7 do only the softmax and the folds.
-// They hand over through mbarriers:
+// ~37 ns with two CTAs per SM), so warp 8 does nothing but wait for each K/V stage,
+// make the generic stores it needs (the chunk's own new rows, zeros past the slice end)
+// and issue the products; warp 9 issues the TMA copies (a tile's copies took its
+// issuing thread ~770 cycles); warps 0-7 do only the softmax and the folds.  They hand
+// over through mbarriers:
+//   stage full (TMA complete_tx) and stage free (tcgen05.commit after the tile's P.V);
 //   S ready (tcgen05.commit, one per S buffer) -> the softmax of tile k;
 //   P ready (256 arrivals, two barriers by tile parity): P of tile k is in TMEM and
-//     O_t of tile k-1 has been read -> the issue warp's P.V of tile k;
-//   P.V done (tcgen05.commit, two by parity) -> the folds, and the issue warp's reuse
-//     of the tile's stage and S buffer.
+//     O_t of tile k-1 has been read -> P.V of tile k;
+//   P.V done (tcgen05.commit, two by parity) -> the folds, and the reuse of the tile's
+//     S buffer.
 // With three S buffers (d = 64) S runs two tiles ahead of P.V, so the threads find
 // each tile's scores ready.  Every wait is bounded; a thread whose wait gives up
 // reports it, stops waiting and still takes part in every barrier, so the CTA ends.
@@ -48,7 +50,7 @@ struct T5Cfg {
     static constexpr int KT = 64;                        // keys per tile
     static constexpr int MP = 128;                       // pairs per CTA (TMEM lanes, MMA M)
     static constexpr int NT = 256;                       // softmax threads (warps 0-7): two per pair
-    static constexpr int NTHREADS = NT + 32;             // + the issue warp
+    static constexpr int NTHREADS = NT + 64;             // + the product warp and the copy warp
     static constexpr int DH = D / 2;                     // output columns per thread
     static constexpr int ST = D == 64 ? 5 : 2;           // K/V stages: two CTAs per SM either way
     static constexpr int NSB = D == 64 ? 3 : 2;          // S / P buffers in TMEM
@@ -60,7 +62,7 @@ struct T5Cfg {
     static constexpr int Q_BYTES = HALVES * QHALF_BYTES;
     static constexpr int PIPE_OFF = Q_BYTES;
     static constexpr int BAR_OFF = PIPE_OFF + ST * STAGE_BYTES;
-    static constexpr int NBAR = ST + NSB + 2 + 2;        // stages, S buffers, P.V done [2], P ready [2]
+    static constexpr int NBAR = 2 * ST + NSB + 2 + 2;    // stage full [ST], stage free [ST], S, P.V done [2], P ready [2]
     static constexpr int SLOT_OFF = BAR_OFF + NBAR * 8;
     static constexpr int PAGE_OFF = (SLOT_OFF + 4 + 15) / 16 * 16;
     static constexpr int XCH_OFF = PAGE_OFF + kSlicePageCap * 4;  // [3][2][MP] floats: row max by tile parity, row sum
@@ -91,14 +93,16 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issuer = warp == C::NT / 32;  // the issue warp
+    const bool issuer = warp == C::NT / 32;        // the product warp
+    const bool copier = warp == C::NT / 32 + 1;    // the copy warp
     const int quarter = warp & 3;            // TMEM lanes [32 quarter, +32): this warp's pairs
     const int half = (warp >> 2) & 1;        // which 32 keys of each tile and which d/2 output columns
     const int prow = quarter * 32 + lane;    // the pair within the CTA (TMEM lane)
     uint8_t *qs = smem;
     uint8_t *pipe = smem + C::PIPE_OFF;
     const uint32_t bar0 = smem_addr(smem + C::BAR_OFF);
-    const uint32_t bar_s = bar0 + 8 * C::ST, bar_o = bar_s + 8 * C::NSB, bar_p = bar_o + 16;
+    const uint32_t bar_free = bar0 + 8 * C::ST, bar_s = bar_free + 8 * C::ST, bar_o = bar_s + 8 * C::NSB,
+                   bar_p = bar_o + 16;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::SLOT_OFF);
     int32_t *page_buf = reinterpret_cast<int32_t *>(smem + C::PAGE_OFF);
     float *xch = reinterpret_cast<float *>(smem + C::XCH_OFF);
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     // this thread's pair (row of every product); the issue warp computes one it never uses
     const int pm = it.pair0 + prow;
     const int qi = pm / G, qh = pm - (pm / G) * G;
-    const bool valid = !issuer && qi < it.rows;
+    const bool valid = warp < C::NT / 32 && qi < it.rows;
     int limit = !valid ? -1 : (p.causal ? it.n_keys - it.rows + qi : it.n_keys - 1);
     limit = min(limit, key_end - 1);  // keys of this CTA's slice only
     // key tiles up to the largest admissible key of the CTA's pairs (rows grow with m)
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     };
 
     if (issuer && lane == 0) {
-        for (int b = 0; b < C::NBAR; ++b) mbar_init(bar0 + 8 * b, b >= C::ST + C::NSB + 2 ? C::NT : 1);
+        for (int b = 0; b < C::NBAR; ++b) mbar_init(bar0 + 8 * b, b >= C::NBAR - 2 ? C::NT : 1);
         fence_barrier_init();
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
@@ -149,7 +153,7 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     const uint32_t t_o = tmem + C::O_COL;
     const uint64_t policy = l2_evict_first_policy();
 
-    // TMA of tile kt's K and V into its stage (issue warp, lane 0)
+    // TMA of tile kt's K and V into its stage (copy warp, lane 0)
     auto issue = [&](int kt) {
         const int s = kt % C::ST;
         const uint32_t kdst = smem_addr(pipe + s * C::STAGE_BYTES);
@@ -181,17 +185,17 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     };
 
     const int pre = ntiles < C::ST ? ntiles : C::ST;
-    if (p.prefetch_pool && issuer && lane == 0)
+    if (p.prefetch_pool && copier && lane == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
     pdl_wait();
     pdl_launch_dependents();
-    if (!p.prefetch_pool && issuer && lane == 0)
+    if (!p.prefetch_pool && copier && lane == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
 
     // ---- Q: the pair rows into the swizzled K-major tile (zeros for no pair).  Each of the
     // two threads of a pair takes chunks c and c + CH/2 (rotate-half partners) for its
     // quarter of c in [0, CH/2).
-    if (!issuer) {
+    if (warp < C::NT / 32) {
         constexpr int CQ = CH / 4;  // first-half chunks per thread
         const T *qrow = static_cast<const T *>(p.q) +
                         (static_cast<size_t>(it.q_row0 + (valid ? qi : 0)) * p.num_qo_heads + it.kv_head * G +
@@ -230,7 +234,6 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
         constexpr uint64_t kmaj = t5::smem_desc_bits(16, 1024);
         constexpr uint64_t vmaj = t5::smem_desc_bits(C::HALF_BYTES, 1024);
         bool live = true;                       // false once one of its waits gave up
-        int tma_issued = pre, tma_waited = 0;   // tiles [0, tma_issued) requested, [0, tma_waited) landed
         int s_issued = -1, pv_issued = -1;      // the last S and P.V committed
         // a bounded wait by the whole warp; the outcome is warp-uniform
         auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -245,7 +248,6 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
         auto stage_s = [&](int kt) {
             const int s = kt % C::ST;
             if (!wait_all(bar0 + 8 * s, (kt / C::ST) & 1)) return;
-            tma_waited = kt + 1;
             uint8_t *kp = pipe + s * C::STAGE_BYTES;
             uint8_t *vp = kp + C::TILE_BYTES;
             const int t0 = key_begin + kt * C::KT;
@@ -310,26 +312,42 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
                     for (int kk = 0; kk < C::KT / 16; ++kk)
                         t5::mma_ts(t_o, t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
                     t5::commit(bar_o + 8 * (kt & 1));
+                    t5::commit(bar_free + 8 * (kt % C::ST));  // the stage is free for the copy warp
                 }
                 pv_issued = kt;
             }
-            // P.V of tile kt - 1 is done: its stage takes tile kt - 1 + ST, and its S buffer
-            // (the last reader of which it was) takes S of tile kt + NSB - 1
-            if (kt >= 1 && live && wait_all(bar_o + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1) &&
-                kt - 1 + C::ST < ntiles) {
-                if (lane == 0) issue(kt - 1 + C::ST);
-                tma_issued = kt - 1 + C::ST + 1;
-            }
-            if (kt + C::NSB - 1 < ntiles && live) stage_s(kt + C::NSB - 1);
+            // S of tile kt + NSB - 1 goes in the S buffer of tile kt - 1, whose P.V (its last
+            // reader) must be done
+            if (kt + C::NSB - 1 < ntiles && live &&
+                (kt == 0 || wait_all(bar_o + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1)))
+                stage_s(kt + C::NSB - 1);
         }
-        // drain what is still in flight (bounded; immediate when every wait succeeded): a
-        // commit arrives once every earlier product of its thread is done, and each barrier
-        // has at most one phase pending
+        // drain what is still in flight (bounded; immediate when every wait succeeded): the
+        // last commit on each barrier, which is the only phase a wait can still name
         if (lane == 0) {
-            if (pv_issued >= 0) mbar_wait_bounded(bar_o + 8 * (pv_issued & 1), (pv_issued >> 1) & 1);
-            if (s_issued >= 0) mbar_wait_bounded(bar_s + 8 * (s_issued % C::NSB), (s_issued / C::NSB) & 1);
-            for (int kt = tma_waited; kt < tma_issued; ++kt)
-                mbar_wait_bounded(bar0 + 8 * (kt % C::ST), (kt / C::ST) & 1);
+            for (int k = max(0, pv_issued - 1); k <= pv_issued; ++k)
+                mbar_wait_bounded(bar_o + 8 * (k & 1), (k >> 1) & 1);
+            for (int k = max(0, pv_issued - C::ST + 1); k <= pv_issued; ++k)
+                mbar_wait_bounded(bar_free + 8 * (k % C::ST), (k / C::ST) & 1);
+            for (int k = max(0, s_issued - C::NSB + 1); k <= s_issued; ++k)
+                mbar_wait_bounded(bar_s + 8 * (k % C::NSB), (k / C::NSB) & 1);
+        }
+    } else if (copier) {
+        // ================= the copy warp =================
+        // Tile j goes in stage j % ST once P.V of tile j - ST, the stage's last reader, is done.
+        if (lane == 0) {
+            int issued = pre;
+            for (int j = pre; j < ntiles; ++j) {
+                if (!mbar_wait_bounded(bar_free + 8 * (j % C::ST), ((j / C::ST) - 1) & 1)) {
+                    atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
+                    break;
+                }
+                issue(j);
+                issued = j + 1;
+            }
+            // drain: the last copy into each stage (bounded; immediate when it was consumed)
+            for (int j = max(0, issued - C::ST); j < issued; ++j)
+                mbar_wait_bounded(bar0 + 8 * (j % C::ST), (j / C::ST) & 1);
         }
     } else {
         // ================= the softmax warps =================
