@@ -128,3 +128,44 @@ def test_prefill_segments(group, head_dim, page_size, dtype, causal, prefill_ker
     out, lse, info = H.gpu_outputs(w, prefill_kernel=prefill_kernel)
     assert info["num_prefill_tiles"] > 0
     H.compare(out, lse, ro, rl, f"prefill/{prefill_kernel} g{group} d{head_dim} ps{page_size} {dtype} causal={causal}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+def test_prefill_key_slices_repeated(prefill_kernel, splits):
+    """A fixed number of key slices per prefill tile (1, 2, 3 and the maximum 8), their
+    partials merged by the merge kernel.  The same plan runs five times, the last
+    three from one CUDA graph, each output checked against the oracle: nothing a call
+    leaves in the plan's buffers may change the next one."""
+    import paged_kv_gqa_05_gb300 as pg
+    w = W.custom("slices", [1536, 40, 700], 64, 14, 2, 64, "bf16", 128, seed=11 + splits,
+                 qo_lens=[300, 1, 129], causal=True)
+    ro, rl = H.oracle_outputs(w)
+    dev = H.to_device(w)
+    plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dev["q"].dtype,
+                   max_batch=w.batch, max_q_rows=w.rows, prefill_kernel=prefill_kernel, prefill_splits=splits)
+    plan.update(w.kv_indptr, w.last_page_len, dev["kv_indices"], w.num_pages, qo_indptr=w.qo_indptr,
+                causal=True, kv_indices_host=w.kv_indices)
+    info = plan.info()
+    assert info["num_prefill_tiles"] > 0
+    assert (info["num_merge_tasks"] > 0) == (splits > 1)
+    out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(dev["q"].shape[:2], dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        out.fill_(float("nan"))
+        plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
+        torch.cuda.synchronize()
+        H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl,
+                  f"{prefill_kernel} {splits} slices, eager")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl,
+                  f"{prefill_kernel} {splits} slices, graph")
+    plan.close()
