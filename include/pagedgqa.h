@@ -139,9 +139,8 @@ typedef struct pgqa_plan_config {
                              0: none */
     int prefill_kernel;   /* requests with several query rows: PGQA_PREFILL_TCGEN05 (5th-
                              generation tensor cores, S and O in tensor memory) or
-                             PGQA_PREFILL_MMA_SYNC; PGQA_PREFILL_AUTO takes tcgen05 for
-                             head_dim 64 and for groups above 8, else mma.sync (the faster
-                             one on GB300 in each case) */
+                             PGQA_PREFILL_MMA_SYNC; PGQA_PREFILL_AUTO takes tcgen05, the
+                             faster one on GB300 at every shape measured */
 } pgqa_plan_config;
 
 #define PGQA_PREFILL_AUTO 0

@@ -388,15 +388,11 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     p->box_rows = std::min(c.page_size, p->tile);
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
     p->stages = c.pipeline_stages == 3 ? 3 : 2;
-    // AUTO takes the kernel measured faster on GB300 for 512-row causal chunks over 1536 keys:
-    // tcgen05 for d 64 (20.6 against 26.1 us; beside a ragged call's 127 decode rows the two
-    // tie) and for 16-head groups at d 128 (51.5 against 60.0 us); mma.sync for d 128 with
-    // groups of up to 8 (28.1 against 31.2 us), where 96 registers a thread make the
-    // tcgen05 kernel spill its 64-column output rows.
-    if (c.prefill_kernel == PGQA_PREFILL_AUTO)
-        p->prefill_kind = (c.head_dim == 64 || group > 8) ? PGQA_PREFILL_TCGEN05 : PGQA_PREFILL_MMA_SYNC;
-    else
-        p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_TCGEN05 ? PGQA_PREFILL_TCGEN05 : PGQA_PREFILL_MMA_SYNC;
+    // AUTO takes the tcgen05 kernel, measured faster on GB300 for 512-row causal chunks over
+    // 1536 keys at every shape tried: d 64 g 7 19.5 against 26.1 us, d 64 g 4 (page 16) 25.8
+    // against 36.4, d 128 g 6 25.5 against 28.1, d 128 g 16 39.4 against 60.0; beside a ragged
+    // call's 127 decode rows 42.1 against 42.5 us.
+    p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_MMA_SYNC ? PGQA_PREFILL_MMA_SYNC : PGQA_PREFILL_TCGEN05;
     p->prefill_pairs = p->prefill_kind == PGQA_PREFILL_MMA_SYNC ? 64 : 128;
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);

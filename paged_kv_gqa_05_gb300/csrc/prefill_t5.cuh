@@ -17,22 +17,25 @@
 //   (the row maximum is the one value they exchange, through shared memory; each keeps
 //   its own partial row sum), and write their P back over S as two 16-bit terms
 //   (P = P_hi + P_lo);
-//   O_t[128 x d] = P_hi . V + P_lo . V   tcgen05.mma with A from TMEM, V MN-major
-//   each thread folds its d/2 columns of the row of O_t into fp32 output registers.
+//   O[128 x d] += P_hi . V + P_lo . V   tcgen05.mma with A from TMEM, V MN-major; O
+//   accumulates over the tiles in TMEM.  The row's running maximum moves only when the
+//   row maximum exceeds it by more than 2^8 (rare after the first tiles); then the two
+//   threads scale their halves of the row of O in TMEM (after P.V of the previous tile)
+//   and their sums.  At the end each thread reads its d/2 columns once and normalises.
 //
 // Warp specialisation.  Issuing a product holds the issuing thread for about as long
 // as the tensor pipe takes to run it (measured on GB300: ~23 ns per 128x64x16 product,
 // ~37 ns with two CTAs per SM), so warp 8 does nothing but wait for each K/V stage,
 // make the generic stores it needs (the chunk's own new rows, zeros past the slice end)
 // and issue the products; warp 9 issues the TMA copies (a tile's copies took its
-// issuing thread ~770 cycles); warps 0-7 do only the softmax and the folds.  They hand
+// issuing thread ~770 cycles); warps 0-7 do only the softmax and the output.  They hand
 // over through mbarriers:
 //   stage full (TMA complete_tx) and stage free (tcgen05.commit after the tile's P.V);
 //   S ready (tcgen05.commit, one per S buffer) -> the softmax of tile k;
-//   P ready (256 arrivals, two barriers by tile parity): P of tile k is in TMEM and
-//     O_t of tile k-1 has been read -> P.V of tile k;
-//   P.V done (tcgen05.commit, two by parity) -> the folds, and the reuse of the tile's
-//     S buffer.
+//   P ready (256 arrivals, two barriers by tile parity): P of tile k (and any scaled
+//     row of O) is in TMEM -> P.V of tile k;
+//   P.V done (tcgen05.commit, two by parity) -> a rescale of O, the final read of O, and
+//     the reuse of the tile's S buffer.
 // With three S buffers (d = 64) S runs two tiles ahead of P.V, so the threads find
 // each tile's scores ready.  Every wait is bounded; a thread whose wait gives up
 // reports it, stops waiting and still takes part in every barrier, so the CTA ends.
@@ -67,7 +70,7 @@ struct T5Cfg {
     static constexpr int PAGE_OFF = (SLOT_OFF + 4 + 15) / 16 * 16;
     static constexpr int XCH_OFF = PAGE_OFF + kSlicePageCap * 4;  // [3][2][MP] floats: row max by tile parity, row sum
     static constexpr int SMEM_BYTES = XCH_OFF + 3 * 2 * MP * 4;
-    // TMEM: NSB S / P buffers of 64 columns, then D columns for O_t; 256 columns leave
+    // TMEM: NSB S / P buffers of 64 columns, then D columns for O; 256 columns leave
     // room for two CTAs per SM.
     static constexpr uint32_t TMEM_COLS = 256;
     static constexpr int S_COL = 0, O_COL = 64 * NSB;
@@ -222,9 +225,6 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     fence_proxy_async_smem();  // generic stores before the products read the tile
     __syncthreads();
 
-    float o[C::DH];  // output columns [DH half, DH half + DH) of this pair's row
-#pragma unroll
-    for (int j = 0; j < C::DH; ++j) o[j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // running row max (scaled log2 units); this thread's partial sum
 
     if (issuer) {
@@ -300,14 +300,15 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
         if (ntiles > 0) stage_s(0);
         if (C::NSB == 3 && ntiles > 1) stage_s(1);
         for (int kt = 0; kt < ntiles; ++kt) {
-            // P of tile kt is in TMEM and every thread has read O_t of tile kt - 1
+            // P of tile kt (and any scaled row of O) is in TMEM
             if (wait_all(bar_p + 8 * (kt & 1), (kt >> 1) & 1)) {
                 if (lane == 0) {
                     const uint32_t vb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES);
                     t5::fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < C::KT / 16; ++kk)
-                        t5::mma_ts(t_o, t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, kk > 0);
+                    for (int kk = 0; kk < C::KT / 16; ++kk)  // O accumulates over the tiles
+                        t5::mma_ts(t_o, t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o,
+                                   kt > 0 || kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < C::KT / 16; ++kk)
                         t5::mma_ts(t_o, t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
@@ -351,23 +352,17 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
         }
     } else {
         // ================= the softmax warps =================
+        // O accumulates over the tiles in TMEM.  The running maximum m_run moves only when a
+        // row's maximum exceeds it by more than 2^8 (P then stays below 256, exact enough in
+        // two 16-bit terms); O and the row sum are then scaled by 2^(m_old - m_new).
+        constexpr float kRescale = 8.f;
         bool live = true;  // false once one of this thread's waits gave up
-        // o = o * a + O_t of tile kt (its own row)
-        auto fold = [&](int kt, float a) {
+        auto wait_pv = [&](int kt) {  // P.V of tile kt is done
             const bool got = live && mbar_wait_bounded(bar_o + 8 * (kt & 1), (kt >> 1) & 1);
             if (!got && live) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
             live = got;
             t5::fence_after();
-#pragma unroll
-            for (int c0 = 0; c0 < C::DH; c0 += 32) {
-                uint32_t r[32];
-                t5::ld32(t_o + lane_base + C::DH * half + c0, r);
-                t5::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(o[c0 + j], a, __uint_as_float(r[j]));
-            }
         };
-        float prev_alpha = 1.f;
         for (int kt = 0; kt < ntiles; ++kt) {
             // ---- S of tile kt: mask, online softmax, P (two 16-bit terms) back over S
             const bool got = live && mbar_wait_bounded(bar_s + 8 * (kt % C::NSB), (kt / C::NSB) & 1);
@@ -398,11 +393,14 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
             float *xc = xch + (kt & 1) * 2 * C::MP;
             xc[half * C::MP + prow] = mx;
             named_bar_sync_id(1 + quarter, 64);
-            mx = fmaxf(mx, xc[(1 - half) * C::MP + prow]);
-            const float mn = fmaxf(m_run, mx * p.scale_log2);  // the scale is positive
-            const float alpha = (mn == m_run) ? 1.f : ex2_approx(m_run - mn);
-            m_run = mn;
-            const float neg_m = (mn == -INFINITY) ? 0.f : -mn;  // a row with no key yet: every P is 0
+            mx = fmaxf(mx, xc[(1 - half) * C::MP + prow]) * p.scale_log2;  // the scale is positive
+            // both threads of a pair take the same decision
+            float alpha = 1.f;
+            if (mx > m_run + kRescale) {  // also the first key of the row (m_run = -inf)
+                if (m_run != -INFINITY) alpha = ex2_approx(m_run - mx);
+                m_run = mx;
+            }
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;  // a row with no key yet: every P is 0
             {
                 uint32_t ph[16], pl[16];
                 float lsum = 0.f;
@@ -419,21 +417,80 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
                 // keys [32 half, +32) are columns [16 half, +16) of P_hi ([0, 32)) and of P_lo ([32, 64))
                 t5::st16(t_s(kt) + lane_base + 16 * half, ph);
                 t5::st16(t_s(kt) + lane_base + 32 + 16 * half, pl);
-                t5::wait_st();
             }
-            // ---- O_t of tile kt - 1 (its product ran during this softmax)
-            if (kt >= 1) fold(kt - 1, prev_alpha);
-            prev_alpha = alpha;
-            // ---- P of tile kt is in TMEM and O_t is read: the issue warp may go on
+            // ---- rows whose maximum moved: O (tiles before kt) scaled once P.V of tile kt - 1 is
+            // done; warp-collective, the other lanes scale by 1
+            if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                wait_pv(kt - 1);
+#pragma unroll
+                for (int c0 = 0; c0 < C::DH; c0 += 32) {
+                    uint32_t r[32];
+                    t5::ld32(t_o + lane_base + C::DH * half + c0, r);
+                    t5::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                    t5::st32(t_o + lane_base + C::DH * half + c0, r);
+                }
+            }
+            t5::wait_st();
+            // ---- P of tile kt (and any scaled O) is in TMEM: the product warp may go on
             t5::fence_before();
             t5::arrive(bar_p + 8 * (kt & 1));
         }
-        if (ntiles > 0) fold(ntiles - 1, prev_alpha);
+        if (ntiles > 0) wait_pv(ntiles - 1);
         // the row sum is the sum of both threads' parts
         float *xl = xch + 2 * 2 * C::MP;
         xl[half * C::MP + prow] = l_run;
         named_bar_sync_id(1 + quarter, 64);
         l_run += xl[(1 - half) * C::MP + prow];
+
+        // ---- normalise and store this thread's columns of its pair's row, read from TMEM
+        // (warp-collective loads; the stores only for pairs that exist)
+        const float L = l_run;
+        // L == 0 only for a row with no admissible key; NaN (a poisoned row) propagates.
+        const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
+        const float lse2 = (L == 0.f) ? -INFINITY : m_run + lg2_approx(L);
+        const bool split_keys = it.part_base >= 0;
+        const size_t slot = split_keys && valid
+                                ? static_cast<size_t>(it.part_base + qi * it.num_splits + it.split) * G + qh
+                                : 0;
+        const size_t row = static_cast<size_t>(it.q_row0 + (valid ? qi : 0)) * p.num_qo_heads + it.kv_head * G + qh;
+#pragma unroll
+        for (int c0 = 0; c0 < C::DH; c0 += 32) {
+            uint32_t r[32];
+            if (ntiles > 0) {  // CTA-uniform
+                t5::ld32(t_o + lane_base + C::DH * half + c0, r);
+                t5::wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+            if (!valid) continue;
+            const int col = C::DH * half + c0;
+            if (split_keys || p.out_dtype == PGQA_FP32) {  // normalised partial, or fp32 rows
+                float4 *dst = reinterpret_cast<float4 *>(split_keys ? p.partial_o + slot * D + col
+                                                                    : static_cast<float *>(p.out) + row * D + col);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    dst[j / 4] = make_float4(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv,
+                                             __uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + row * D + col);
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    dst[j / 8] = make_uint4(
+                        M::pack(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv),
+                        M::pack(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv),
+                        M::pack(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv),
+                        M::pack(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv));
+            }
+        }
+        if (valid && half == 0) {
+            if (split_keys)  // its log2-sum-exp, for the merge
+                p.partial_lse[slot] = lse2;
+            else if (p.lse != nullptr)
+                p.lse[row] = lse2 * 0.6931471805599453f;
+        }
     }
 
     // ---- fused append: the split-0 CTA holding pair (i, head 0) stores row i's new K/V
@@ -468,35 +525,6 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
         t5::dealloc(tmem, C::TMEM_COLS);
     }
 
-    // ---- normalise and store this thread's columns of its pair's row
-    if (!valid) return;
-    const float L = l_run;
-    // L == 0 only for a row with no admissible key; NaN (a poisoned row) propagates.
-    const float inv = (L == 0.f) ? 0.f : rcp_approx(L);
-    const float lse2 = (L == 0.f) ? -INFINITY : m_run + lg2_approx(L);
-    if (it.part_base >= 0) {  // split keys: normalised partial + its log2-sum-exp
-        const size_t slot = static_cast<size_t>(it.part_base + qi * it.num_splits + it.split) * G + qh;
-        float4 *dst = reinterpret_cast<float4 *>(p.partial_o + slot * D + C::DH * half);
-#pragma unroll
-        for (int j = 0; j < C::DH; j += 4)
-            dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
-        if (half == 0) p.partial_lse[slot] = lse2;
-        return;
-    }
-    const size_t row = static_cast<size_t>(it.q_row0 + qi) * p.num_qo_heads + it.kv_head * G + qh;
-    if (p.out_dtype == PGQA_FP32) {
-        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * D + C::DH * half);
-#pragma unroll
-        for (int j = 0; j < C::DH; j += 4)
-            dst[j / 4] = make_float4(o[j] * inv, o[j + 1] * inv, o[j + 2] * inv, o[j + 3] * inv);
-    } else {
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + row * D + C::DH * half);
-#pragma unroll
-        for (int j = 0; j < C::DH; j += 8)
-            dst[j / 8] = make_uint4(M::pack(o[j] * inv, o[j + 1] * inv), M::pack(o[j + 2] * inv, o[j + 3] * inv),
-                                    M::pack(o[j + 4] * inv, o[j + 5] * inv), M::pack(o[j + 6] * inv, o[j + 7] * inv));
-    }
-    if (half == 0 && p.lse != nullptr) p.lse[row] = lse2 * 0.6931471805599453f;
 }
 
 template <int D, bool ROPE, typename T>
