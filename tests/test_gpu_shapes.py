@@ -169,3 +169,27 @@ def test_prefill_key_slices_repeated(prefill_kernel, splits):
         H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl,
                   f"{prefill_kernel} {splits} slices, graph")
     plan.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("head_dim,group", [(64, 7), (128, 6)])
+def test_prefill_growing_scores(prefill_kernel, head_dim, group):
+    """Keys scaled up tile by tile (x(1 + 3 t) for the 64-key tile t of each request), so
+    a row's maximum jumps far past its running maximum again and again: this drives the
+    tcgen05 kernel's rescale of O in tensor memory on many tiles (random scores seldom
+    move the maximum by the 2^8 that triggers it), and the mma.sync kernel's online
+    rescale alike."""
+    w = W.custom("grow", [1100, 300, 70], 64, group, 1, head_dim, "bf16", 64, seed=5 + head_dim,
+                 qo_lens=[260, 1, 70], causal=True)
+    ps = w.page_size
+    for b in range(w.batch):
+        p0, p1 = int(w.kv_indptr[b]), int(w.kv_indptr[b + 1])
+        n = (p1 - p0 - 1) * ps + int(w.last_page_len[b]) if p1 > p0 else 0
+        for j in range(n):
+            page = int(w.kv_indices[p0 + j // ps])
+            w.k_pool[page, j % ps] = (w.k_pool[page, j % ps].float() * (1 + 3 * (j // 64))).to(w.k_pool.dtype)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, info = H.gpu_outputs(w, prefill_kernel=prefill_kernel)
+    assert info["num_prefill_tiles"] > 0
+    H.compare(out, lse, ro, rl, f"growing scores {prefill_kernel} d{head_dim} g{group}")
