@@ -339,12 +339,85 @@ def run_ours(args, rank, world, local):
         update_plan()
         replay("step")
 
-    # e2e: pinned host copies of every step's inputs in and outputs out
+    # e2e: pinned host copies of every step's inputs in and outputs out.  With graphs the
+    # copies are pipelined with the layers: layer l's inputs go up on one copy stream and
+    # layer l waits only for them; its output comes down on another as soon as it is done.
     host_in = torch.empty(L["inputs"].shape, dtype=dt, pin_memory=True)
     host_in.copy_(L["inputs"])
     host_out = torch.empty(L["out"].shape, dtype=dt, pin_memory=True)
+    per_layer_in = L["inputs"].numel() // layers
+
+    h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def chunks(n, first_sizes):
+        """[a, b) layer ranges: the given sizes first, then doubling, to n."""
+        out, a, size = [], 0, 1
+        for sz in first_sizes:
+            if a >= n:
+                break
+            out.append((a, min(n, a + sz)))
+            a, size = out[-1][1], sz
+        while a < n:
+            size *= 2
+            out.append((a, min(n, a + size)))
+            a = out[-1][1]
+        return out
+
+    # inputs: layer 0 alone, then doubling chunks that stay ahead of the layers; outputs:
+    # large chunks early and a one-layer chunk last, so little is left after the last layer
+    in_chunks = chunks(layers, [1, 1])
+    out_chunks = [(layers - b, layers - a) for a, b in reversed(chunks(layers, [1, 1]))]
+
+    def e2e_calls():
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        h2d.wait_event(fork)
+        d2h.wait_event(fork)
+        ev_in = {}
+        with torch.cuda.stream(h2d):
+            for a, b in in_chunks:
+                sl = slice(a * per_layer_in, b * per_layer_in)
+                L["inputs"][sl].copy_(host_in[sl], non_blocking=True)
+                ev_in[a] = torch.cuda.Event()
+                ev_in[a].record(h2d)
+        ev_done = {}
+        for l in range(layers):
+            if l in ev_in:
+                stream.wait_event(ev_in[l])
+            if fused:
+                pg.append_run(plan.handle, L["k_new"][l], L["v_new"][l], L["q"][l], L["k_pool"][l],
+                              L["v_pool"][l], out=L["out"][l], pool_stable=True, stream=stream)
+            else:
+                if L["slots"] is not None and positions is not None:
+                    plan.kv_append_rope(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l],
+                                        L["slots"], positions, stream=stream)
+                elif L["slots"] is not None:
+                    pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
+                                 stream=stream)
+                pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l], stream=stream)
+            if any(b == l + 1 for _, b in out_chunks):
+                ev_done[l + 1] = torch.cuda.Event()
+                ev_done[l + 1].record(stream)
+        with torch.cuda.stream(d2h):
+            for a, b in out_chunks:
+                d2h.wait_event(ev_done[b])
+                host_out[a:b].copy_(L["out"][a:b], non_blocking=True)
+        join = torch.cuda.Event()
+        join.record(d2h)
+        stream.wait_event(join)
+
+    if graphs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_calls()
+        graphs["e2e"] = g
+        torch.cuda.synchronize()
 
     def e2e_step():
+        if graphs:
+            update_plan()
+            graphs["e2e"].replay()
+            return
         L["inputs"].copy_(host_in, non_blocking=True)
         step()
         host_out.copy_(L["out"], non_blocking=True)
