@@ -451,6 +451,15 @@ def run_ours(args, rank, world, local):
     t_e2e = max_over_ranks(timed(e2e_step, args.steps), world, device)
     clocks = sampler.stop()
 
+    # host time of one plan update (validation, work list, one staged H2D copy), GPU idle
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        for _ in range(50):
+            update_plan()
+        plan_us = (time.perf_counter() - t0) / 50 * 1e6
+    torch.cuda.synchronize()
+
     flags = pg.read_device_flags()
     if flags:
         raise RuntimeError(f"device-side check fired during the benchmark: flags={flags}")
@@ -526,6 +535,7 @@ def run_ours(args, rank, world, local):
         },
         "us_per_layer": round(t_dev / args.steps / layers * 1e6, 3),
         "us_per_run_call": round(t_run / (run_reps * layers) * 1e6, 3),
+        "plan_update_host_us": round(plan_us, 2),
         "us_per_decode_launch": round(per_launch_s * 1e6, 3),
         "pct_of_peak": round(100.0 * value / peak, 2),
         "bytes": b,
@@ -591,9 +601,19 @@ def cpu_baseline(w, seconds: float) -> dict:
         el = time.perf_counter() - t0
         if el >= seconds or reps >= 1000:
             break
+    # the same oracle on one thread, over a quarter of the time
+    reps1, t1 = 0, time.perf_counter()
+    while True:
+        _oracle_layer(w, orc, 1, sub)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= seconds / 4 or reps1 >= 1000:
+            break
     return {"value": round(sub.bytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"one layer of {w.name} ({sub.n} requests), fp64 oracle repeated {reps} times "
-                      f"over {el:.1f} s on {cores} threads"}
+                      f"over {el:.1f} s on {cores} threads",
+            "single_thread": {"value": round(sub.bytes * reps1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{reps1} repetitions over {el1:.1f} s on 1 thread"}}
 
 
 def run_reference(args, rank, world):
