@@ -435,6 +435,15 @@ def run_ours(args, rank, world, local):
         barrier(world)
         return start.elapsed_time(end) / 1e3  # seconds
 
+    # Untimed burn-in before the warm-up steps: ~0.3 s of steps brings a GPU that was idle
+    # (a fresh box) to its working clocks; the first timed run on one was 11 % slow without it.
+    burn_in, t_b = 0, time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_b < 0.3:
+            for _ in range(20):
+                step()
+            burn_in += 20
+            torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -526,7 +535,8 @@ def run_ours(args, rank, world, local):
             "num_qo_heads": w.num_qo_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "kv_tokens": int(w.kv_lens.sum()),
             "l2": f"inputs larger than L2: {layers} independent layer pools per step",
-            "graph": not args.no_graph, "parallelism": "replicas" if world > 1 else "single",
+            "graph": not args.no_graph, "burn_in_steps": burn_in,
+            "parallelism": "replicas" if world > 1 else "single",
             "decode_kernel": args.decode_kernel, "append_mode": args.append_mode if L["slots"] is not None else None,
             "rope_theta": args.rope_theta if args.rope_theta > 0 else None,
             "prefill_kernel": args.prefill_kernel if w.qo_indptr is not None else None,
