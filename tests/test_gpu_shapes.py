@@ -193,3 +193,26 @@ def test_prefill_growing_scores(prefill_kernel, head_dim, group):
     out, lse, info = H.gpu_outputs(w, prefill_kernel=prefill_kernel)
     assert info["num_prefill_tiles"] > 0
     H.compare(out, lse, ro, rl, f"growing scores {prefill_kernel} d{head_dim} g{group}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("prefill_kernel", ["tcgen05", "mma_sync"])
+def test_long_chunk_sampled_rows(prefill_kernel):
+    """The suite's largest prefill launch: one 3000-row causal chunk over 4000 keys
+    (d 128, g 8, page 64; 375 tiles of 64 or 188 of 128 (row, head) pairs per kv head
+    before key slicing), checked on sampled (row, head) pairs that the oracle computes
+    one by one: the first rows, the last row and random ones, across both kv heads."""
+    import oracle
+    w = W.custom("long_chunk", [4000], 64, 16, 2, 128, "bf16", 80, seed=31, qo_lens=[3000], causal=True)
+    out, lse, info = H.gpu_outputs(w, prefill_kernel=prefill_kernel)
+    assert info["num_prefill_tiles"] > 0
+    orc = oracle.get()
+    rng = np.random.default_rng(7)
+    rows = [0, 1, 2, 1499, 2999] + [int(x) for x in rng.integers(0, 3000, 8)]
+    for r in rows:
+        for h in (0, 5, 7, 8, 13, 15):
+            o, l = orc.attention_partial(W.raw16(w.q), W.raw16(w.k_pool), W.raw16(w.v_pool), w.kv_indptr,
+                                         w.kv_indices, w.last_page_len, w.dtype, 0, r, h, 0, 4000,
+                                         qo_indptr=w.qo_indptr, causal=True)
+            assert np.abs(out[r, h] - o).max() <= H.MAX_ABS, (prefill_kernel, r, h)
+            assert abs(lse[r, h] - l) <= H.LSE_ABS, (prefill_kernel, r, h)
