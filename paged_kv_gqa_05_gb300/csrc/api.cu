@@ -491,12 +491,30 @@ static constexpr double kSaturatedRate = 5300.0;  // bytes / ns
 static constexpr double kWaveCostNs = 1500.0;     // CTA set-up + epilogue, per wave of CTAs
 static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any row is split
 
+// Pipeline depth of the tensor-core decode kernel: three stages when every warp's tiles
+// of the longest slice can be requested at once (the whole slice in flight from the
+// start), or when the grid fits one wave at two CTAs per SM, its slices are long (at
+// least twice what three stages hold) and no prefill grid shares the GPU: measured on
+// GB300, 32 mixed d 128 -4 %, 64 x 2049 at g = 16 -6 %, 4 x 32k even, while 224-key slices
+// (1 x 32k) lost 8 % and the ragged call, whose decode rows then went unsplit, 9 %.
+// Otherwise two, so that three CTAs fit on an SM and overlap each other's set-up and
+// epilogue.
+static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items, bool with_prefill) {
+    const int64_t held = 3LL * kDecodeWarps * plan->tile;  // keys three stages hold
+    if (max_slice <= held) return 3;
+    if (!with_prefill && max_slice >= 2 * held &&
+        n_items <= static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[3])
+        return 3;
+    return 2;
+}
+
 // Slice length (whole warp tiles, at least one tile per warp) for the decode rows that
 // minimises the estimated launch time.  The hardware runs `slots` CTAs at once and
 // starts the rest (longest first) as slots free up, so the estimate walks waves of
 // `slots` items: each wave takes max(its bytes / rate(CTAs in it), its longest slice /
 // one CTA's rate), plus kWaveCostNs; splitting adds kMergeCostNs.
-static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_rows, int64_t longest) {
+static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_rows, int64_t longest,
+                            bool with_prefill) {
     const pgqa_plan_config &c = plan->cfg;
     const int64_t tile = plan->tile;
     const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
@@ -542,8 +560,8 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
             max_slice = std::max(max_slice, std::min(sl, n));
             split = split || ns > 1;
         }
-        const int stages = c.pipeline_stages != 0 ? c.pipeline_stages
-                                                  : (max_slice <= 3LL * kDecodeWarps * tile ? 3 : 2);
+        const int stages =
+            c.pipeline_stages != 0 ? c.pipeline_stages : pick_stages(plan, max_slice, n_items, with_prefill);
         const int64_t slots = static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[stages];
         if (have && (n_items > 8 * slots || n_items > plan->max_items)) break;
         const double cr = cta_rate(c.head_dim, plan->group, stages);
@@ -681,7 +699,8 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     int64_t longest = 0;
     for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
     const int64_t ls = c.split_tokens > 0 ? round_up(c.split_tokens, tile)
-                                          : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest);
+                                          : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest,
+                                                         !prefill.empty());
 
     std::vector<WorkItem> items;
     std::vector<MergeTask> tasks;
@@ -800,13 +819,10 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     plan->staged_used[buf] = true;
     plan->cur ^= 1;
 
-    // Pipeline depth: three stages when every warp's tiles of the longest slice can be
-    // requested at once (the whole slice in flight from the start), two otherwise so
-    // that three CTAs fit on an SM and overlap each other's set-up and epilogue.
     if (c.pipeline_stages == 0) {
         int64_t longest_item = 0;
         for (const WorkItem &w : items) longest_item = std::max<int64_t>(longest_item, w.tok_end - w.tok_begin);
-        plan->stages = longest_item <= 3LL * kDecodeWarps * tile ? 3 : 2;
+        plan->stages = pick_stages(plan, longest_item, static_cast<int64_t>(items.size()), !prefill.empty());
     }
     plan->n_items = static_cast<int>(items.size());
     plan->n_prefill = static_cast<int>(prefill.size());
