@@ -493,17 +493,18 @@ static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any 
 
 // Pipeline depth of the tensor-core decode kernel: three stages when every warp's tiles
 // of the longest slice can be requested at once (the whole slice in flight from the
-// start), or when the grid fits one wave at two CTAs per SM, its slices are long (at
-// least twice what three stages hold) and no prefill grid shares the GPU: measured on
-// GB300, 32 mixed d 128 -4 %, 64 x 2049 at g = 16 -6 %, 4 x 32k even, while 224-key slices
-// (1 x 32k) lost 8 % and the ragged call, whose decode rows then went unsplit, 9 %.
-// Otherwise two, so that three CTAs fit on an SM and overlap each other's set-up and
-// epilogue.
+// start), or when the grid is less than one full wave at two CTAs per SM (so some SMs
+// run a single CTA), its slices are long (at least twice what three stages hold) and no
+// prefill grid shares the GPU.  Measured on GB300: 32 mixed d 128 (292 CTAs) -4 %,
+// 64 x 2049 at g = 16 (256 CTAs) -6 %; a full wave (4 x 32k, 304 CTAs) ran its launch 6 %
+// slower, 224-key slices (1 x 32k) lost 8 %, and a ragged call, whose decode rows then went
+// unsplit, 9 %.  Otherwise two, so that three CTAs fit on an SM and overlap each other's
+// set-up and epilogue.
 static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items, bool with_prefill) {
     const int64_t held = 3LL * kDecodeWarps * plan->tile;  // keys three stages hold
     if (max_slice <= held) return 3;
     if (!with_prefill && max_slice >= 2 * held &&
-        n_items <= static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[3])
+        n_items < static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[3])
         return 3;
     return 2;
 }
