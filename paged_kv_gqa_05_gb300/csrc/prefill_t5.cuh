@@ -84,8 +84,8 @@ __device__ __forceinline__ uint32_t swz_off(int r, int c, int half_bytes) {
     return (c >> 3) * half_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-// Two CTAs per SM: 18 warps put five on some of the SM's four sub-partitions, whose
-// 16K registers then allow 96 a thread.
+// Two CTAs per SM: 20 warps, five on each of the SM's four sub-partitions, whose 16K
+// registers then allow 96 a thread (102, rounded down to the allocation unit of 8).
 template <int D, bool ROPE, typename T>
 __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     prefill_t5_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     const int key_begin = it.key_begin, key_end = it.key_end;
     const bool fused = p.k_new != nullptr;
     const int new_begin = it.n_keys - it.rows;  // the chunk's own keys (a fused call supplies them)
-    // this thread's pair (row of every product); the issue warp computes one it never uses
+    // this thread's pair (row of every product); the product and copy warps compute one they never use
     const int pm = it.pair0 + prow;
     const int qi = pm / G, qh = pm - (pm / G) * G;
     const bool valid = warp < C::NT / 32 && qi < it.rows;
