@@ -50,6 +50,13 @@ MUTANTS = {
                             "const double a = x[base + i], b = x[base + (i + half + 1) % d];"),
     "rope_second_sign": ("y[base + i + half] = b * c + a * s;", "y[base + i + half] = b * c - a * s;"),
     "rope_first_position": ("const double pos = (double)positions[r];", "const double pos = (double)positions[0];"),
+    # more attention, merge and decoding mistakes
+    "causal_global_row": ("int64_t i = r - r0;\n        int64_t allowed = n;", "int64_t i = r;\n        int64_t allowed = n;"),
+    "kv_len_full_last_page": ("return (npages - 1) * page_size + last_page_len[b];", "return npages * page_size;"),
+    "gather_first_kv_head": ("int64_t base = ((page * page_size + off) * Hkv + kvh) * (int64_t)d;",
+                             "int64_t base = ((page * page_size + off) * Hkv + 0) * (int64_t)d;"),
+    "merge_uniform_weights": ("double w = exp(lse_parts[s] - m) / z;", "double w = 1.0 / n;"),
+    "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
 }
 
 
