@@ -7,7 +7,8 @@
  * found through a CSR page table.  Work is split along each request's history
  * ("split-KV"); a partial (output, log-sum-exp) is computed per slice in
  * parallel and the partials are merged.  A paged KV append writes new tokens'
- * rows into the pool.
+ * rows into the pool.  A ragged call also serves requests with several query
+ * rows (a chunked prefill): their rows attend causally, bottom-right aligned.
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers unless the parameter name ends in _host.
@@ -128,7 +129,9 @@ typedef struct pgqa_plan_config {
     int decode_kernel;    /* PGQA_DECODE_AUTO (tensor cores), PGQA_DECODE_TENSOR_CORE or
                              PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
     int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
-                             per plan_update (3 when a whole slice fits in flight, else 2) */
+                             per plan_update: 3 when a whole slice fits in flight, or when a
+                             grid of long slices is less than one wave at two CTAs per SM and
+                             no prefill segment shares the call; else 2 */
     int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
     int decode_ctas;      /* tensor-core decode: 0 = one CTA per work item (the default);
                              n > 0 = n persistent CTAs walking the work list; -1 = one
