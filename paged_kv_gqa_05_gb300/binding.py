@@ -334,6 +334,12 @@ class Plan:
             plan_destroy(self.handle)
             self.handle = None
 
+    def __enter__(self) -> "Plan":
+        return self
+
+    def __exit__(self, *exc) -> None:
+        self.close()
+
     def __del__(self):
         try:
             self.close()

@@ -113,27 +113,26 @@ def test_split_rows_repeated_calls(kernel_opts):
     ro, rl = H.oracle_outputs(w)
     dev = H.to_device(w)
     pg.kv_append(dev["k_pool"], dev["v_pool"], dev["k_new"], dev["v_new"], dev["slot_mapping"])
-    plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dev["q"].dtype,
-                   max_batch=w.batch, max_q_rows=w.rows, split_tokens=128, **kernel_opts)
-    plan.update(w.kv_indptr, w.last_page_len, dev["kv_indices"], w.num_pages, kv_indices_host=w.kv_indices)
-    info = plan.info()
-    # split rows: 700, 1500, 2048 and 3000 keys (6, 12, 16, 24 slices), two kv heads each
-    assert info["num_merge_tasks"] == 2 * 4 and info["max_splits_used"] == 24
-    out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
-    lse = torch.empty(dev["q"].shape[:2], dtype=torch.float32, device="cuda")
-    for _ in range(3):
-        out.fill_(float("nan"))
-        plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
-        torch.cuda.synchronize()
-        H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"splits {kernel_opts}")
-    s = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
-    for _ in range(2):
-        out.fill_(float("nan"))
-        g.replay()
-        torch.cuda.synchronize()
-        H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"splits {kernel_opts} graph")
-    plan.close()
+    with pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dev["q"].dtype,
+                 max_batch=w.batch, max_q_rows=w.rows, split_tokens=128, **kernel_opts) as plan:
+        plan.update(w.kv_indptr, w.last_page_len, dev["kv_indices"], w.num_pages, kv_indices_host=w.kv_indices)
+        info = plan.info()
+        # split rows: 700, 1500, 2048 and 3000 keys (6, 12, 16, 24 slices), two kv heads each
+        assert info["num_merge_tasks"] == 2 * 4 and info["max_splits_used"] == 24
+        out = torch.empty(dev["q"].shape, dtype=torch.float32, device="cuda")
+        lse = torch.empty(dev["q"].shape[:2], dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            out.fill_(float("nan"))
+            plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
+            torch.cuda.synchronize()
+            H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"splits {kernel_opts}")
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse)
+        for _ in range(2):
+            out.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"splits {kernel_opts} graph")
     assert pg.read_device_flags() == 0
