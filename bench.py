@@ -3,9 +3,10 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 plan_update (host, once per step) and, for each of the workload's independent
-layer pools, kv_append of the step's new tokens followed by run() (split-KV
-partial kernel + merge where a row is split).  The per-layer calls are replayed
-from one CUDA graph.  With 24 (or 28) independent pools the inputs of a step
+layer pools, append_run(): the step's new tokens appended and attended in one
+launch (split-KV partial kernel, + merge where a row is split; --append-mode
+separate runs kv_append, then run()).  The per-layer calls are replayed from one
+CUDA graph.  With 24 (or 28) independent pools the inputs of a step
 are several times larger than L2, so every step reads K/V from HBM.
 
 Default workload: 128 requests x (300 cached + 1 appended) tokens, page 16,
@@ -504,7 +505,7 @@ def run_ours(args, rank, world, local):
         roofline = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak, "unit": "TFLOP/s",
                     "frac": round(tf / tpeak, 4), "traffic": None, "peak_source": tpeak_src,
                     "algorithmic_flops_per_launch": flops,
-                    "kernel": ("prefill_t5_kernel" if args.prefill_kernel == "tcgen05" else "prefill_tc_kernel")
+                    "kernel": ("prefill_tc_kernel" if args.prefill_kernel == "mma_sync" else "prefill_t5_kernel")
                               + (" (+ merge_kernel)" if info["num_merge_tasks"] else ""),
                     "timing": timing_note}
     else:
