@@ -216,3 +216,28 @@ def test_long_chunk_sampled_rows(prefill_kernel):
                                          qo_indptr=w.qo_indptr, causal=True)
             assert np.abs(out[r, h] - o).max() <= H.MAX_ABS, (prefill_kernel, r, h)
             assert abs(lse[r, h] - l) <= H.LSE_ABS, (prefill_kernel, r, h)
+
+
+@pytest.mark.gpu
+def test_zero_sized_calls():
+    """Empty calls are accepted and do nothing: an append of zero tokens (plain and
+    rotating), and a plan over zero requests run on zero query rows."""
+    import paged_kv_gqa_05_gb300 as pg
+    g = torch.Generator(device="cuda").manual_seed(3)
+    k_pool = torch.randn(4, 16, 2, 64, device="cuda", generator=g).to(torch.bfloat16)
+    v_pool = torch.randn(4, 16, 2, 64, device="cuda", generator=g).to(torch.bfloat16)
+    before_k, before_v = k_pool.clone(), v_pool.clone()
+    empty = torch.empty(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    slots = torch.empty(0, dtype=torch.int64, device="cuda")
+    pg.kv_append(k_pool, v_pool, empty, empty, slots)
+    with pg.Plan(14, 2, 64, 16, torch.bfloat16, max_batch=4, max_q_rows=4, rope_theta=1e6,
+                 rope_max_position=64) as plan:
+        plan.kv_append_rope(k_pool, v_pool, empty, empty, slots, torch.empty(0, dtype=torch.int32, device="cuda"))
+        plan.update(np.zeros(1, np.int32), np.zeros(0, np.int32), torch.empty(0, dtype=torch.int32, device="cuda"), 4)
+        info = plan.info()
+        assert info["num_items"] == 0 and info["num_prefill_tiles"] == 0 and info["total_q_rows"] == 0
+        out = plan.run(torch.empty(0, 14, 64, dtype=torch.bfloat16, device="cuda"), k_pool, v_pool)
+        assert out.shape == (0, 14, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(k_pool, before_k) and torch.equal(v_pool, before_v)
+    assert pg.read_device_flags() == 0
