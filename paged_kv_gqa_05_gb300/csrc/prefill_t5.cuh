@@ -402,18 +402,24 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
             }
             const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;  // a row with no key yet: every P is 0
             {
+                // key pairs through packed fp32x2 arithmetic (fewer issue slots, which the
+                // product warp on the same sub-partition needs)
                 uint32_t ph[16], pl[16];
-                float lsum = 0.f;
+                const uint64_t scale2 = t5::f2(p.scale_log2, p.scale_log2), negm2 = t5::f2(neg_m, neg_m);
+                uint64_t lsum2 = t5::f2(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2_approx(fmaf(sc[2 * j], p.scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(sc[2 * j + 1], p.scale_log2, neg_m));
-                    lsum += p0 + p1;
-                    ph[j] = M::pack(p0, p1);
+                    const float2 x = t5::f2_split(t5::f2_fma(t5::f2(sc[2 * j], sc[2 * j + 1]), scale2, negm2));
+                    const uint64_t p01 = t5::f2(ex2_approx(x.x), ex2_approx(x.y));
+                    lsum2 = t5::f2_add(lsum2, p01);
+                    const float2 pv = t5::f2_split(p01);
+                    ph[j] = M::pack(pv.x, pv.y);
                     const float2 f = unpack2<T>(ph[j]);
-                    pl[j] = M::pack(p0 - f.x, p1 - f.y);
+                    const float2 lo = t5::f2_split(t5::f2_sub(p01, t5::f2(f.x, f.y)));
+                    pl[j] = M::pack(lo.x, lo.y);
                 }
-                l_run = l_run * alpha + lsum;
+                const float2 ls = t5::f2_split(lsum2);
+                l_run = l_run * alpha + (ls.x + ls.y);
                 // keys [32 half, +32) are columns [16 half, +16) of P_hi ([0, 32)) and of P_lo ([32, 64))
                 t5::st16(t_s(kt) + lane_base + 16 * half, ph);
                 t5::st16(t_s(kt) + lane_base + 32 + 16 * half, pl);
