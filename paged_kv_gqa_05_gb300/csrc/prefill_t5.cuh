@@ -284,14 +284,15 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                const uint32_t kb = smem_addr(kp);
+                // descriptors as base + offset / 16: the start-address field cannot carry (shared
+                // memory is below 2^18 bytes), so each product costs one add per operand
+                const uint64_t qd = t5::smem_desc(smem_addr(qs), kmaj), kd = t5::smem_desc(smem_addr(kp), kmaj);
                 t5::fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t kofs = (ks >> 2) * C::HALF_BYTES + (ks & 3) * 32;
                     const uint32_t qofs = (ks >> 2) * C::QHALF_BYTES + (ks & 3) * 32;
-                    t5::mma_ss(t_s(kt), t5::smem_desc(smem_addr(qs) + qofs, kmaj), t5::smem_desc(kb + kofs, kmaj),
-                               id_s, ks > 0);
+                    t5::mma_ss(t_s(kt), qd + (qofs >> 4), kd + (kofs >> 4), id_s, ks > 0);
                 }
                 t5::commit(bar_s + 8 * (kt % C::NSB));
             }
@@ -303,15 +304,15 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
             // P of tile kt (and any scaled row of O) is in TMEM
             if (wait_all(bar_p + 8 * (kt & 1), (kt >> 1) & 1)) {
                 if (lane == 0) {
-                    const uint32_t vb = smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES);
+                    const uint64_t vd = t5::smem_desc(smem_addr(pipe + (kt % C::ST) * C::STAGE_BYTES + C::TILE_BYTES), vmaj);
+                    const uint32_t ts = t_s(kt);
                     t5::fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::KT / 16; ++kk)  // O accumulates over the tiles
-                        t5::mma_ts(t_o, t_s(kt) + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o,
-                                   kt > 0 || kk > 0);
+                        t5::mma_ts(t_o, ts + 8 * kk, vd + kk * (2048 >> 4), id_o, kt > 0 || kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < C::KT / 16; ++kk)
-                        t5::mma_ts(t_o, t_s(kt) + 32 + 8 * kk, t5::smem_desc(vb + kk * 2048, vmaj), id_o, true);
+                        t5::mma_ts(t_o, ts + 32 + 8 * kk, vd + kk * (2048 >> 4), id_o, true);
                     t5::commit(bar_o + 8 * (kt & 1));
                     t5::commit(bar_free + 8 * (kt % C::ST));  // the stage is free for the copy warp
                 }
