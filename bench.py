@@ -83,18 +83,22 @@ def sum_over_ranks(value: float, world: int, device=None) -> float:
 # peaks and clocks
 # ---------------------------------------------------------------------------
 
-PROFILE_FILES = {"qwen05_decode": "decode_tc_qwen05_decode_128x301.md",
-                 "long_context_b4": "decode_tc_long_context_b4_32768.md"}
-KERNEL_SOURCES = ("paged_kv_gqa_05_gb300/csrc/decode_tc.cuh", "paged_kv_gqa_05_gb300/csrc/common.cuh")
+DECODE_SOURCES = ("paged_kv_gqa_05_gb300/csrc/decode_tc.cuh", "paged_kv_gqa_05_gb300/csrc/common.cuh")
+PREFILL_SOURCES = DECODE_SOURCES + ("paged_kv_gqa_05_gb300/csrc/tcgen05.cuh",
+                                    "paged_kv_gqa_05_gb300/csrc/prefill_t5.cuh")
+# workload -> (ncu summary under profiles/, the sources of the kernel it describes)
+PROFILE_FILES = {"qwen05_decode": ("decode_tc_qwen05_decode_128x301.md", DECODE_SOURCES),
+                 "long_context_b4": ("decode_tc_long_context_b4_32768.md", DECODE_SOURCES),
+                 "prefill_chunk": ("prefill_t5_prefill_chunk_512x1536.md", PREFILL_SOURCES)}
 
 
-def kernel_sources_hash() -> str:
-    """Hash of the decode kernel's sources: decode_tc.cuh and common.cuh without the block
-    of host-side launcher declarations (which does not change the compiled kernel)."""
+def kernel_sources_hash(sources=DECODE_SOURCES) -> str:
+    """Hash of a kernel's sources, with common.cuh's block of host-side launcher
+    declarations left out (it does not change the compiled kernel)."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             text = fh.read()
         if f.endswith("common.cuh"):
@@ -107,9 +111,9 @@ def kernel_sources_hash() -> str:
 def profiled_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when there is
     none for this workload or the kernel source changed after it was taken."""
-    name = PROFILE_FILES.get(workload)
-    if not name:
+    if workload not in PROFILE_FILES:
         return None
+    name, sources = PROFILE_FILES[workload]
     fields = {}
     try:
         with open(os.path.join(ROOT, "profiles", name)) as f:
@@ -119,7 +123,7 @@ def profiled_traffic(workload: str):
                     fields[k.strip()] = v.strip()
     except OSError:
         return None
-    if fields.get("kernel_sources_sha256_16") != kernel_sources_hash():
+    if fields.get("kernel_sources_sha256_16") != kernel_sources_hash(sources):
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])
@@ -503,7 +507,7 @@ def run_ours(args, rank, world, local):
         tpeak, tpeak_src = bf16_peak()
         tf = flops / per_launch_s / 1e12
         roofline = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": round(tf / tpeak, 4), "traffic": None, "peak_source": tpeak_src,
+                    "frac": round(tf / tpeak, 4), "traffic": traffic, "peak_source": tpeak_src,
                     "algorithmic_flops_per_launch": flops,
                     "kernel": ("prefill_tc_kernel" if args.prefill_kernel == "mma_sync" else "prefill_t5_kernel")
                               + (" (+ merge_kernel)" if info["num_merge_tasks"] else ""),

@@ -69,3 +69,23 @@ def test_warmup_floor():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--warmup", "2"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_profiled_traffic_lookup(tmp_path, monkeypatch):
+    """The roofline's traffic comes from a committed ncu summary only while the
+    summary's source hash matches the kernel's sources; otherwise it is null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for workload, (name, sources) in bench.PROFILE_FILES.items():
+        assert os.path.exists(os.path.join(ROOT, "profiles", name)), name
+        assert all(os.path.exists(os.path.join(ROOT, f)) for f in sources)
+    assert bench.profiled_traffic("tiny") is None
+    # a summary whose hash no longer matches the sources gives no traffic
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "x.md").write_text("traffic_bytes_per_launch: 123\nkernel_sources_sha256_16: 0\n")
+    monkeypatch.setattr(bench, "PROFILE_FILES", {"w": ("x.md", bench.DECODE_SOURCES)})
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_hash", lambda sources=(): "0")
+    assert bench.profiled_traffic("w") == 123
+    monkeypatch.setattr(bench, "kernel_sources_hash", lambda sources=(): "1")
+    assert bench.profiled_traffic("w") is None
