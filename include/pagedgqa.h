@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define PGQA_ABI_VERSION 3
+#define PGQA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define PGQA_API __attribute__((visibility("default")))
@@ -351,6 +351,86 @@ typedef struct pgqa_plan_info {
 } pgqa_plan_info;
 
 PGQA_API pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info);
+
+/*
+ * pgqa_plan_schedule -- the schedule pgqa_plan_update would build, computed on
+ * the host alone.
+ *
+ * Runs the checks and the split heuristic of pgqa_plan_update (split-KV as in
+ * "A library kernel for decode", section "What changed"; the ragged form of
+ * the "flashlet" README, design bullets) for a GPU with num_sms SMs, and
+ * returns the work lists instead of uploading them.  It touches no device and
+ * allocates nothing on one, so it runs on a machine without a GPU: to see how
+ * a batch will be cut, or to size a plan, before any launch.
+ *
+ *   cfg                 plan options, checked as pgqa_plan_create checks them.
+ *                       The heuristic assumes cfg->ctas_per_sm CTA slots per
+ *                       SM, or 2 when it is 0 (what every decode kernel
+ *                       variant has on GB300, so the schedule equals the one
+ *                       a plan on a GB300 with the same num_sms builds).
+ *   num_sms             SMs of the target GPU (152 on GB300), >= 1
+ *   kv_indptr_host, last_page_len_host, qo_indptr_host, batch, num_pages,
+ *   causal              as for pgqa_plan_update
+ *   kv_indices_host     [kv_indptr[batch]] int32, HOST: checked against
+ *                       [0, num_pages) like pgqa_plan_update's host mirror
+ *   slices, max_slices  caller-owned host array, or NULL (then only counted):
+ *                       one entry per decode CTA, in launch order
+ *   merges, max_merges  as above, one entry per merged (query row, kv head)
+ *   tiles, max_tiles    as above, one entry per prefill-segment CTA
+ *   info                out: the counts and decisions (always written when
+ *                       the table passes its checks)
+ *
+ * Errors: every status pgqa_plan_create and pgqa_plan_update return for the
+ * same options and table (no PGQA_ERR_CUDA); PGQA_ERR_CAPACITY also when a
+ * non-NULL array holds fewer entries than the schedule has (info still says
+ * how many).
+ */
+typedef struct pgqa_slice {
+    int32_t q_row;         /* query row */
+    int32_t kv_head;
+    int32_t key_begin;     /* keys [key_begin, key_end) of the row's request; key_begin is */
+    int32_t key_end;       /*   a multiple of the kernel's warp tile (32 keys at head_dim 64, else 16) */
+    int32_t partial_slot;  /* -1: the CTA writes the (row, kv head) output; else the split partial it fills */
+    int32_t append_pos;    /* pgqa_append_run: key position whose new K/V row this CTA stores, or -1 */
+} pgqa_slice;
+
+typedef struct pgqa_merge {
+    int32_t q_row;
+    int32_t kv_head;
+    int32_t slot_base;     /* partials slot_base .. slot_base + num_splits - 1 are merged */
+    int32_t num_splits;
+} pgqa_merge;
+
+typedef struct pgqa_prefill_tile {
+    int32_t q_row0;        /* first query row of the request */
+    int32_t rows;          /* L, the request's query rows */
+    int32_t n_keys;        /* N, the request's keys */
+    int32_t kv_head;
+    int32_t pair0;         /* first (row, head) pair of the tile; pair m = i * G + h for row */
+    int32_t pairs;         /*   q_row0 + i and head h of the group; the tile holds up to `pairs` */
+    int32_t key_begin;     /* key slice [key_begin, key_end) of this CTA */
+    int32_t key_end;
+    int32_t partial_base;  /* -1: final rows; else partial of (row i, split s) is partial_base + i * num_splits + s */
+    int32_t split;         /* s */
+    int32_t num_splits;
+} pgqa_prefill_tile;
+
+typedef struct pgqa_schedule_info {
+    int num_items;          /* decode CTAs (slices) */
+    int num_merge_tasks;
+    int num_prefill_tiles;
+    int split_tokens;       /* slice length chosen for the decode rows */
+    int max_splits_used;    /* most slices any (row, kv head) got */
+    int pipeline_stages;    /* the tensor-core decode kernel's depth, 2 or 3 */
+    int total_q_rows;
+    int64_t kv_tokens;      /* sum of kv_len over requests */
+} pgqa_schedule_info;
+
+PGQA_API pgqa_status pgqa_plan_schedule(const pgqa_plan_config *cfg, int num_sms, const int32_t *kv_indptr_host,
+                                        const int32_t *last_page_len_host, const int32_t *qo_indptr_host, int batch,
+                                        const int32_t *kv_indices_host, int64_t num_pages, int causal,
+                                        pgqa_slice *slices, int max_slices, pgqa_merge *merges, int max_merges,
+                                        pgqa_prefill_tile *tiles, int max_tiles, pgqa_schedule_info *info);
 
 #ifdef __cplusplus
 }

@@ -17,5 +17,4 @@ requests with several query rows (a prefill chunk) ride along with decode rows.
 """
 from .binding import (BF16, FP16, FP32, POOL_STABLE, PagedGQAError, Plan, append_run,  # noqa: F401
                       decode_static_scratch, kv_append, kv_append_rope, load, plan_create, plan_destroy,
-                      plan_get_info,
-                      plan_update, read_device_flags, run)
+                      plan_get_info, plan_schedule, plan_update, read_device_flags, run)

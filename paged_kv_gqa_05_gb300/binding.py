@@ -2,7 +2,7 @@
 
 The functions carry the C ABI's names without the ``pgqa_`` prefix:
 ``kv_append``, ``plan_create``, ``plan_update``, ``run``, ``plan_destroy``,
-``plan_get_info``, ``read_device_flags``.  Every step of the computation runs in
+``plan_get_info``, ``plan_schedule``, ``read_device_flags``.  Every step of the computation runs in
 the library's CUDA kernels; torch only supplies device memory and the stream.
 There is no fallback: if the shared library is missing or fails to load, every
 call raises.
@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "PGQA_OK", 1: "PGQA_ERR_INVALID_ARG", 2: "PGQA_ERR_UNSUPPORTE
 EXPORTS = ("pgqa_abi_version", "pgqa_status_string", "pgqa_last_error", "pgqa_read_device_flags",
            "pgqa_kv_append", "pgqa_plan_create", "pgqa_plan_update", "pgqa_run",
            "pgqa_plan_destroy", "pgqa_plan_get_info", "pgqa_append_run", "pgqa_decode_static_scratch",
-           "pgqa_kv_append_rope")
+           "pgqa_kv_append_rope", "pgqa_plan_schedule")
 
 
 class PagedGQAError(RuntimeError):
@@ -57,6 +57,20 @@ class PlanInfo(ctypes.Structure):
                 ("total_q_rows", ctypes.c_int), ("num_sms", ctypes.c_int),
                 ("kv_tokens", ctypes.c_int64), ("num_prefill_tiles", ctypes.c_int)]
 
+
+class ScheduleInfo(ctypes.Structure):
+    _fields_ = [("num_items", ctypes.c_int), ("num_merge_tasks", ctypes.c_int),
+                ("num_prefill_tiles", ctypes.c_int), ("split_tokens", ctypes.c_int),
+                ("max_splits_used", ctypes.c_int), ("pipeline_stages", ctypes.c_int),
+                ("total_q_rows", ctypes.c_int), ("kv_tokens", ctypes.c_int64)]
+
+
+# Rows of pgqa_plan_schedule's output arrays (pgqa_slice, pgqa_merge, pgqa_prefill_tile): int32 fields.
+SLICE_DTYPE = np.dtype([(f, np.int32) for f in ("q_row", "kv_head", "key_begin", "key_end", "partial_slot",
+                                                 "append_pos")])
+MERGE_DTYPE = np.dtype([(f, np.int32) for f in ("q_row", "kv_head", "slot_base", "num_splits")])
+TILE_DTYPE = np.dtype([(f, np.int32) for f in ("q_row0", "rows", "n_keys", "kv_head", "pair0", "pairs", "key_begin",
+                                                "key_end", "partial_base", "split", "num_splits")])
 
 _lib: Optional[ctypes.CDLL] = None
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -103,7 +117,11 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_plan_destroy.argtypes = [_vp]
     lib.pgqa_plan_get_info.restype = ctypes.c_int
     lib.pgqa_plan_get_info.argtypes = [_vp, ctypes.POINTER(PlanInfo)]
-    if lib.pgqa_abi_version() != 3:
+    lib.pgqa_plan_schedule.restype = ctypes.c_int
+    lib.pgqa_plan_schedule.argtypes = [ctypes.POINTER(PlanConfig), ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int,
+                                       _i32p, ctypes.c_int64, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int,
+                                       _vp, ctypes.c_int, ctypes.POINTER(ScheduleInfo)]
+    if lib.pgqa_abi_version() != 4:
         raise RuntimeError("libpagedgqa.so ABI version mismatch")
     _lib = lib
     return lib
@@ -181,6 +199,17 @@ def kv_append_rope(plan: int, k_pool: torch.Tensor, v_pool: torch.Tensor, k: tor
                                       _dev(positions, "positions"), k.shape[0], _stream(stream)))
 
 
+def _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits=0,
+            split_tokens=0, ctas_per_sm=0, decode_kernel="auto", pipeline_stages=0, prefill_splits=0,
+            decode_ctas=0, rope_theta=0.0, rope_max_position=0, prefill_kernel="auto") -> PlanConfig:
+    kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
+    pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
+    return PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
+                      max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
+                      pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta),
+                      pf_kinds[prefill_kernel])
+
+
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
@@ -190,12 +219,9 @@ def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: 
     decode_kernel: "auto" | "tensor_core" | "cuda_core"; rope_theta > 0 turns on the
     rotary embedding of q and the appended K rows (positions < rope_max_position);
     prefill_kernel: "auto" | "tcgen05" | "mma_sync"."""
-    kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
-    pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
-    cfg = PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
-                     max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
-                     pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta),
-                     pf_kinds[prefill_kernel])
+    cfg = _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits,
+                  split_tokens, ctas_per_sm, decode_kernel, pipeline_stages, prefill_splits, decode_ctas,
+                  rope_theta, rope_max_position, prefill_kernel)
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value
@@ -279,6 +305,44 @@ def decode_static_scratch(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
         q.shape[0], P, ps, q.shape[1], Hkv, D, TORCH_TO_CODE[q.dtype], int(splits), _dev(out, "out"),
         TORCH_TO_CODE[out.dtype], None if lse is None else _dev(lse, "lse"), float(sm_scale), _stream(stream)))
     return out
+
+
+def plan_schedule(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int, dtype: torch.dtype,
+                  kv_indptr, last_page_len, kv_indices, num_pages: int, qo_indptr=None, causal: bool = False,
+                  num_sms: int = 152, max_batch: Optional[int] = None, max_q_rows: Optional[int] = None,
+                  **options) -> dict:
+    """pgqa_plan_schedule: the schedule plan_update would build, on the host alone
+    (no GPU needed).  All arrays are host int32; options as for plan_create.
+    Returns {"info": {...}, "slices", "merges", "tiles"} with numpy structured arrays
+    (SLICE_DTYPE, MERGE_DTYPE, TILE_DTYPE) in launch order."""
+    indptr = _host_i32(kv_indptr, "kv_indptr")
+    last = _host_i32(last_page_len, "last_page_len")
+    qo = _host_i32(qo_indptr, "qo_indptr")
+    idx = _host_i32(kv_indices, "kv_indices")
+    batch = len(indptr) - 1
+    rows = batch if qo is None else (int(qo[-1]) if len(qo) else 0)
+    cfg = _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype,
+                  max(1, batch) if max_batch is None else max_batch,
+                  max(1, rows) if max_q_rows is None else max_q_rows, **options)
+    lib = load()
+    info = ScheduleInfo()
+
+    def call(slices, merges, tiles):
+        def ptr(a):
+            return None if a is None else a.ctypes.data
+        _check(lib.pgqa_plan_schedule(ctypes.byref(cfg), int(num_sms), _i32ptr(indptr), _i32ptr(last), _i32ptr(qo),
+                                      batch, _i32ptr(idx if idx is not None and idx.size else None), int(num_pages),
+                                      int(bool(causal)), ptr(slices), 0 if slices is None else len(slices),
+                                      ptr(merges), 0 if merges is None else len(merges), ptr(tiles),
+                                      0 if tiles is None else len(tiles), ctypes.byref(info)))
+
+    call(None, None, None)  # counts
+    slices = np.zeros(info.num_items, SLICE_DTYPE)
+    merges = np.zeros(info.num_merge_tasks, MERGE_DTYPE)
+    tiles = np.zeros(info.num_prefill_tiles, TILE_DTYPE)
+    call(slices, merges, tiles)
+    return {"info": {name: getattr(info, name) for name, _ in ScheduleInfo._fields_},
+            "slices": slices, "merges": merges, "tiles": tiles}
 
 
 def plan_destroy(plan: int) -> None:

@@ -344,10 +344,8 @@ pgqa_status pgqa_kv_append_rope(const pgqa_plan *plan, void *k_pool, void *v_poo
     return PGQA_OK;
 }
 
-pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
-    if (!out || !cfg) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
-    *out = nullptr;
-    const pgqa_plan_config &c = *cfg;
+// Plan options that plan_create accepts (all host-side).
+static pgqa_status check_config(const pgqa_plan_config &c) {
     if (c.num_kv_heads < 1 || c.num_qo_heads < 1 || c.num_qo_heads % c.num_kv_heads != 0)
         return fail(PGQA_ERR_INVALID_ARG, "num_qo_heads %d must be a positive multiple of num_kv_heads %d",
                     c.num_qo_heads, c.num_kv_heads);
@@ -379,11 +377,13 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         if (c.decode_kernel == PGQA_DECODE_CUDA_CORE)
             return fail(PGQA_ERR_UNSUPPORTED, "RoPE runs on the tensor-core kernels");
     }
+    return PGQA_OK;
+}
 
-    pgqa_plan *p = new (std::nothrow) pgqa_plan();
-    if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
+// The plan's host-side shape: kernel choices and tile sizes that follow from the options.
+static void plan_shape(pgqa_plan *p, const pgqa_plan_config &c) {
     p->cfg = c;
-    p->group = group;
+    p->group = c.num_qo_heads / c.num_kv_heads;
     p->tile = decode_warp_tile(c.head_dim);
     p->box_rows = std::min(c.page_size, p->tile);
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
@@ -394,6 +394,33 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     // call's 127 decode rows 42.1 against 42.5 us.
     p->prefill_kind = c.prefill_kernel == PGQA_PREFILL_MMA_SYNC ? PGQA_PREFILL_MMA_SYNC : PGQA_PREFILL_TCGEN05;
     p->prefill_pairs = p->prefill_kind == PGQA_PREFILL_MMA_SYNC ? 64 : 128;
+}
+
+// Capacities of the plan's lists, from its options, SM count and CTA slots per SM.
+static pgqa_status plan_capacity(pgqa_plan *p) {
+    const pgqa_plan_config &c = p->cfg;
+    p->ctas_per_sm = std::max(p->slots_per_sm[2], p->slots_per_sm[3]);
+    // Slices never exceed 8 waves of CTAs + one per row and kv head; forced short slices may need more.
+    const int64_t items = c.max_q_rows * c.num_kv_heads + 8LL * p->num_sms * p->ctas_per_sm + 64;
+    if (items > (1 << 26)) return fail(PGQA_ERR_CAPACITY, "plan capacity too large");
+    p->max_items = static_cast<int>(items);
+    p->max_tasks = static_cast<int>(c.max_q_rows * c.num_kv_heads);
+    p->max_prefill = static_cast<int>((c.max_q_rows * p->group / 64 + c.max_batch + 1) * c.num_kv_heads * 8);
+    // partial slots: split decode slices, plus up to 8 key slices per prefill row and kv head
+    p->max_slots = p->max_items + static_cast<int>(c.max_q_rows * c.num_kv_heads * 8);
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
+    if (!out || !cfg) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
+    *out = nullptr;
+    const pgqa_plan_config &c = *cfg;
+    const pgqa_status cs = check_config(c);
+    if (cs != PGQA_OK) return cs;
+    const int group = c.num_qo_heads / c.num_kv_heads;
+    pgqa_plan *p = new (std::nothrow) pgqa_plan();
+    if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
+    plan_shape(p, c);
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     // CTA slots of the split heuristic, unless the caller fixes them: the resident CTAs
@@ -415,18 +442,11 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
         plan_free(p);
         return cuda_fail(e, "device query");
     }
-    p->ctas_per_sm = std::max(p->slots_per_sm[2], p->slots_per_sm[3]);
-    // Slices never exceed 8 waves of CTAs + one per row and kv head; forced short slices may need more.
-    const int64_t items = c.max_q_rows * c.num_kv_heads + 8LL * p->num_sms * p->ctas_per_sm + 64;
-    if (items > (1 << 26)) {
+    const pgqa_status ps = plan_capacity(p);
+    if (ps != PGQA_OK) {
         plan_free(p);
-        return fail(PGQA_ERR_CAPACITY, "plan capacity too large");
+        return ps;
     }
-    p->max_items = static_cast<int>(items);
-    p->max_tasks = static_cast<int>(c.max_q_rows * c.num_kv_heads);
-    p->max_prefill = static_cast<int>((c.max_q_rows * group / 64 + c.max_batch + 1) * c.num_kv_heads * 8);
-    // partial slots: split decode slices, plus up to 8 key slices per prefill row and kv head
-    p->max_slots = p->max_items + static_cast<int>(c.max_q_rows * c.num_kv_heads * 8);
     const size_t meta = sizeof(WorkItem) * p->max_items + sizeof(MergeTask) * p->max_tasks +
                         sizeof(PrefillItem) * p->max_prefill;
     e = cudaMalloc(&p->d_meta, meta);
@@ -604,12 +624,21 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
     return best_len;
 }
 
-pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
-                             const int32_t *qo_indptr, int batch, const int32_t *kv_indices,
-                             const int32_t *kv_indices_host, int64_t num_pages, int causal,
-                             pgqa_stream_t stream) {
-    if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
-    plan->valid = false;
+// What plan_update builds, computed on the host alone: the table's checks, the
+// decode work list (slices of every (row, kv head)), the merge list, the prefill
+// tiles and the decode kernel's pipeline depth.
+struct Schedule {
+    std::vector<WorkItem> items;
+    std::vector<MergeTask> tasks;
+    std::vector<PrefillItem> prefill;
+    int64_t split_tokens = 0, rows = 0, kv_tokens = 0;
+    int max_used = 1, max_task_splits = 0, stages = 2;
+    bool fusable = true;
+};
+
+static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
+                                  const int32_t *qo_indptr, int batch, bool have_indices,
+                                  const int32_t *kv_indices_host, int64_t num_pages, int causal, Schedule *out) {
     const pgqa_plan_config &c = plan->cfg;
     if (batch < 0 || num_pages < 0) return fail(PGQA_ERR_INVALID_ARG, "negative batch or num_pages");
     if (batch > c.max_batch) return fail(PGQA_ERR_CAPACITY, "batch %d > max_batch %d", batch, c.max_batch);
@@ -628,7 +657,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         if (np * c.page_size >= (int64_t(1) << 30)) return fail(PGQA_ERR_UNSUPPORTED, "request %d too long", b);
     }
     const int64_t nnz = batch > 0 ? kv_indptr[batch] : 0;
-    if (nnz > 0 && !kv_indices) return fail(PGQA_ERR_INVALID_ARG, "kv_indices is NULL");
+    if (nnz > 0 && !have_indices) return fail(PGQA_ERR_INVALID_ARG, "kv_indices is NULL");
     if (kv_indices_host)
         for (int64_t i = 0; i < nnz; ++i)
             if (kv_indices_host[i] < 0 || kv_indices_host[i] >= num_pages)
@@ -659,7 +688,7 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         const int64_t L = r1 - r0;
         // A fused append writes the request's last L key positions from the L new rows.
         if (L > n) fusable = false;
-        if (plan->rope_cs != nullptr && L > 0) {
+        if (c.rope_theta > 0.0 && L > 0) {
             // query rows sit at the request's last L key positions, all in the table
             if (L > n)
                 return fail(PGQA_ERR_INVALID_ARG, "request %d: %lld query rows over %lld keys have no rotary position",
@@ -791,6 +820,39 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
         return a.key_end - a.key_begin > b.key_end - b.key_begin;
     });
 
+    int stages = c.pipeline_stages;
+    if (stages == 0) {
+        int64_t longest_item = 0;
+        for (const WorkItem &w : items) longest_item = std::max<int64_t>(longest_item, w.tok_end - w.tok_begin);
+        stages = pick_stages(plan, longest_item, static_cast<int64_t>(items.size()), !prefill.empty());
+    }
+    out->items.swap(items);
+    out->tasks.swap(tasks);
+    out->prefill.swap(prefill);
+    out->split_tokens = ls;
+    out->rows = rows;
+    out->kv_tokens = kv_tokens;
+    out->max_used = max_used;
+    out->max_task_splits = max_task_splits;
+    out->stages = stages;
+    out->fusable = fusable;
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
+                             const int32_t *qo_indptr, int batch, const int32_t *kv_indices,
+                             const int32_t *kv_indices_host, int64_t num_pages, int causal,
+                             pgqa_stream_t stream) {
+    if (!plan) return fail(PGQA_ERR_INVALID_ARG, "plan is NULL");
+    plan->valid = false;
+    Schedule sc;
+    const pgqa_status ss = build_schedule(plan, kv_indptr, last_page_len, qo_indptr, batch, kv_indices != nullptr,
+                                          kv_indices_host, num_pages, causal, &sc);
+    if (ss != PGQA_OK) return ss;
+    const std::vector<WorkItem> &items = sc.items;
+    const std::vector<MergeTask> &tasks = sc.tasks;
+    const std::vector<PrefillItem> &prefill = sc.prefill;
+
     // Stage in pinned memory (double-buffered) and copy into the persistent buffer.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int buf = plan->cur;
@@ -820,24 +882,79 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     plan->staged_used[buf] = true;
     plan->cur ^= 1;
 
-    if (c.pipeline_stages == 0) {
-        int64_t longest_item = 0;
-        for (const WorkItem &w : items) longest_item = std::max<int64_t>(longest_item, w.tok_end - w.tok_begin);
-        plan->stages = pick_stages(plan, longest_item, static_cast<int64_t>(items.size()), !prefill.empty());
-    }
+    plan->stages = sc.stages;
     plan->n_items = static_cast<int>(items.size());
     plan->n_prefill = static_cast<int>(prefill.size());
     plan->causal = causal != 0;
     plan->n_tasks = static_cast<int>(tasks.size());
-    plan->split_tokens = static_cast<int>(ls);
-    plan->max_splits_used = max_used;
-    plan->max_task_splits = max_task_splits;
-    plan->total_q_rows = static_cast<int>(rows);
-    plan->kv_tokens = kv_tokens;
+    plan->split_tokens = static_cast<int>(sc.split_tokens);
+    plan->max_splits_used = sc.max_used;
+    plan->max_task_splits = sc.max_task_splits;
+    plan->total_q_rows = static_cast<int>(sc.rows);
+    plan->kv_tokens = sc.kv_tokens;
     plan->num_pages = num_pages;
     plan->kv_indices = kv_indices;
-    plan->fusable = fusable;
+    plan->fusable = sc.fusable;
     plan->valid = true;
+    return PGQA_OK;
+}
+
+pgqa_status pgqa_plan_schedule(const pgqa_plan_config *cfg, int num_sms, const int32_t *kv_indptr,
+                               const int32_t *last_page_len, const int32_t *qo_indptr, int batch,
+                               const int32_t *kv_indices, int64_t num_pages, int causal, pgqa_slice *slices,
+                               int max_slices, pgqa_merge *merges, int max_merges, pgqa_prefill_tile *tiles,
+                               int max_tiles, pgqa_schedule_info *info) {
+    if (!cfg || !info) return fail(PGQA_ERR_INVALID_ARG, "NULL argument");
+    if (num_sms < 1) return fail(PGQA_ERR_INVALID_ARG, "num_sms %d", num_sms);
+    if (max_slices < 0 || max_merges < 0 || max_tiles < 0) return fail(PGQA_ERR_INVALID_ARG, "negative array size");
+    const pgqa_status cs = check_config(*cfg);
+    if (cs != PGQA_OK) return cs;
+    // A host-only plan: its shape and capacities as pgqa_plan_create sets them on a GPU
+    // with num_sms SMs, where every decode variant keeps two CTAs resident per SM.
+    pgqa_plan *p = new (std::nothrow) pgqa_plan();
+    if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
+    plan_shape(p, *cfg);
+    p->num_sms = num_sms;
+    p->slots_per_sm[2] = p->slots_per_sm[3] = cfg->ctas_per_sm > 0 ? cfg->ctas_per_sm : 2;
+    Schedule sc;
+    pgqa_status st = plan_capacity(p);
+    if (st == PGQA_OK)
+        st = build_schedule(p, kv_indptr, last_page_len, qo_indptr, batch, kv_indices != nullptr, kv_indices,
+                            num_pages, causal, &sc);
+    const int pairs = p->prefill_pairs;
+    delete p;
+    if (st != PGQA_OK) return st;
+
+    info->num_items = static_cast<int>(sc.items.size());
+    info->num_merge_tasks = static_cast<int>(sc.tasks.size());
+    info->num_prefill_tiles = static_cast<int>(sc.prefill.size());
+    info->split_tokens = static_cast<int>(sc.split_tokens);
+    info->max_splits_used = sc.max_used;
+    info->pipeline_stages = sc.stages;
+    info->total_q_rows = static_cast<int>(sc.rows);
+    info->kv_tokens = sc.kv_tokens;
+    if ((slices && max_slices < info->num_items) || (merges && max_merges < info->num_merge_tasks) ||
+        (tiles && max_tiles < info->num_prefill_tiles))
+        return fail(PGQA_ERR_CAPACITY, "output arrays hold %d / %d / %d entries, the schedule has %d / %d / %d",
+                    max_slices, max_merges, max_tiles, info->num_items, info->num_merge_tasks,
+                    info->num_prefill_tiles);
+    if (slices)
+        for (size_t i = 0; i < sc.items.size(); ++i) {
+            const WorkItem &w = sc.items[i];
+            slices[i] = {w.q_row, w.kv_head, w.tok_begin, w.tok_end, w.out_slot < 0 ? -1 : w.out_slot,
+                         w.write_pos};
+        }
+    if (merges)
+        for (size_t i = 0; i < sc.tasks.size(); ++i) {
+            const MergeTask &t = sc.tasks[i];
+            merges[i] = {t.q_row, t.kv_head, t.slot_base, t.num_splits};
+        }
+    if (tiles)
+        for (size_t i = 0; i < sc.prefill.size(); ++i) {
+            const PrefillItem &t = sc.prefill[i];
+            tiles[i] = {t.q_row0, t.rows, t.n_keys, t.kv_head, t.pair0, pairs, t.key_begin, t.key_end,
+                        t.part_base < 0 ? -1 : t.part_base, t.split, t.num_splits};
+        }
     return PGQA_OK;
 }
 
