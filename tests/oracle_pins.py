@@ -358,6 +358,9 @@ def pin_page_table_checks(orc):
     assert orc.check_page_table([0, 2, 3], [0, 5, 1], [0, 1], 8, 4) != 0, "last_page_len 0"
     assert orc.check_page_table([0, 2, 1], [0, 5, 1], [4, 1], 8, 4) != 0, "indptr not monotone"
     assert orc.check_page_table([0, 0, 1], [3], [0, 2], 8, 4) == 0, "empty request"
+    assert orc.check_page_table([0, 0, 1], [3], [1, 2], 8, 4) != 0, "no pages but last_page_len 1"
+    assert orc.check_page_table([0, 2, 3], [0, -1, 1], [4, 1], 8, 4) != 0, "negative index"
+    assert orc.check_page_table([0, 2, 3], [0, 7, 1], [4, 1], 8, 4) == 0, "last page of the pool"
 
 
 def pin_empty_request(orc):

@@ -58,6 +58,14 @@ MUTANTS = {
                              "int64_t base = ((page * page_size + off) * Hkv + 0) * (int64_t)d;"),
     "merge_uniform_weights": ("double w = exp(lse_parts[s] - m) / z;", "double w = 1.0 / n;"),
     "fp16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
+    # page-table checks, the append's skip rule, empty slices and the merge loop
+    "page_check_pool_end": ("kv_indices[i] >= num_pages)", "kv_indices[i] > num_pages)"),
+    "page_check_negative_index": ("if (kv_indices[i] < 0 || kv_indices[i]", "if (kv_indices[i]"),
+    "page_check_empty_len": ("if (npages == 0 && last_page_len[b] != 0)", "if (npages == 0 && last_page_len[b] < 0)"),
+    "append_skips_slot_zero": ("if (s < 0)\n            continue;", "if (s <= 0)\n            continue;"),
+    "empty_range_lse_zero": ("*lse = -INFINITY;\n        return ORACLE_OK;", "*lse = 0.0;\n        return ORACLE_OK;"),
+    "merge_skips_first": ("for (int s = 0; s < n; ++s) {\n        if (lse_parts[s] == -INFINITY)",
+                          "for (int s = 1; s < n; ++s) {\n        if (lse_parts[s] == -INFINITY)"),
 }
 
 
