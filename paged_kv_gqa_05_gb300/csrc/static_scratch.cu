@@ -1,8 +1,11 @@
 // Split-KV decode for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA graph
-// that is being captured, allocator-free embedded runtimes, or processes whose
-// device memory is fully owned by another allocator.  For them,
+// Some callers of this code cannot call cudaMalloc: processes whose device memory
+// is reserved up front and handed out by another allocator (a framework's caching
+// allocator or an arena sized at start-up), where an allocation outside it fails
+// or fragments that reserve; and embedded or real-time hosts that forbid
+// allocation after initialisation, because cudaMalloc and cudaFree may block or
+// synchronise the device at unpredictable times.  For them,
 // pgqa_decode_static_scratch runs the same decode path (the tensor-core partial
 // kernel and the log-sum-exp merge) with every intermediate buffer -- the work
 // list, the merge list and the split partials -- carved out of one file-scope
@@ -51,9 +54,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // One thread per (request, kv head, slice): an even cut of the request's keys
 // into `splits` slices of whole warp tiles, read from the device page table.
+// The table is checked here, where it is first read: a request whose page range
+// [kv_indptr[b], kv_indptr[b+1]) is negative, decreasing or reaches past the
+// num_indices entries of kv_indices, or that has no pages but a non-zero
+// last_page_len, raises PGQA_FLAG_PAGE_INDEX and gets no keys, so no kernel reads
+// kv_indices outside [0, num_indices).  A last_page_len outside [1, page_size]
+// for a request with pages is clamped and raises the same flag.
 __global__ void build_static_work(const int32_t *__restrict__ kv_indptr, const int32_t *__restrict__ last_page_len,
-                                  int batch, int num_kv_heads, int splits, int page_size, int tile,
-                                  WorkItem *items, MergeTask *tasks, unsigned int *flags) {
+                                  int64_t num_indices, int batch, int num_kv_heads, int splits, int page_size,
+                                  int tile, WorkItem *items, MergeTask *tasks, unsigned int *flags) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int total = batch * num_kv_heads * splits;
     if (i >= total) return;
@@ -61,19 +70,30 @@ __global__ void build_static_work(const int32_t *__restrict__ kv_indptr, const i
     const int t = i / splits;
     const int kvh = t % num_kv_heads;
     const int b = t / num_kv_heads;
-    const int np = kv_indptr[b + 1] - kv_indptr[b];
+    const int p0 = kv_indptr[b], p1 = kv_indptr[b + 1];
     int last = last_page_len[b];
-    if (np > 0 && (last < 1 || last > page_size)) {
-        atomicOr(flags, PGQA_FLAG_PAGE_INDEX);
-        last = last < 1 ? 1 : page_size;
+    bool bad = p0 < 0 || p1 < p0 || static_cast<int64_t>(p1) > num_indices;
+    const int np = bad ? 0 : p1 - p0;
+    if (np == 0 && last != 0) bad = true;  // no pages means no keys: last_page_len must be 0
+    int n = 0;
+    if (!bad && np > 0) {
+        if (last < 1 || last > page_size) {
+            if (s == 0 && kvh == 0) atomicOr(flags, PGQA_FLAG_PAGE_INDEX);
+            last = last < 1 ? 1 : page_size;
+        }
+        const int64_t n64 = static_cast<int64_t>(np - 1) * page_size + last;
+        if (n64 > INT_MAX / 2)
+            bad = true;  // a key count the 32-bit slice bounds cannot hold
+        else
+            n = static_cast<int>(n64);
     }
-    const int n = np <= 0 ? 0 : (np - 1) * page_size + last;
+    if (bad && s == 0 && kvh == 0) atomicOr(flags, PGQA_FLAG_PAGE_INDEX);
     const int per = (n + splits - 1) / splits;
     const int len = ((per + tile - 1) / tile) * tile;
     const int tb = min(n, s * len);
     const int te = min(n, (s + 1) * len);
     WorkItem w;
-    w.page_base = kv_indptr[b];
+    w.page_base = bad ? 0 : p0;
     w.tok_begin = tb;
     w.tok_end = te;
     w.q_row = b;
@@ -95,11 +115,13 @@ using namespace pgqa;
 
 extern "C" PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const void *k_pool, const void *v_pool,
                                                   const int32_t *kv_indptr, const int32_t *kv_indices,
-                                                  const int32_t *last_page_len, int batch, int64_t num_pages,
+                                                  int64_t num_indices, const int32_t *last_page_len, int batch,
+                                                  int64_t num_pages,
                                                   int page_size, int num_qo_heads, int num_kv_heads, int head_dim,
                                                   pgqa_dtype dtype, int splits, void *out, pgqa_dtype out_dtype,
                                                   float *lse, float sm_scale, pgqa_stream_t stream) {
-    if (batch < 0 || num_pages < 0) return report(PGQA_ERR_INVALID_ARG, "negative batch or num_pages");
+    if (batch < 0 || num_pages < 0 || num_indices < 0)
+        return report(PGQA_ERR_INVALID_ARG, "negative batch, num_pages or num_indices");
     if (num_kv_heads < 1 || num_qo_heads < 1 || num_qo_heads % num_kv_heads != 0)
         return report(PGQA_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
     const int group = num_qo_heads / num_kv_heads;
@@ -114,7 +136,8 @@ extern "C" PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const 
     if (num_pages * static_cast<int64_t>(page_size) >= (int64_t(1) << 31))
         return report(PGQA_ERR_UNSUPPORTED, "pool rows must stay below 2^31");
     if (batch == 0) return PGQA_OK;
-    if (!q || !k_pool || !v_pool || !kv_indptr || !kv_indices || !last_page_len || !out)
+    // kv_indices may be NULL only when it has no entries (every request then has no keys).
+    if (!q || !k_pool || !v_pool || !kv_indptr || !last_page_len || !out || (!kv_indices && num_indices > 0))
         return report(PGQA_ERR_INVALID_ARG, "NULL pointer");
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
          reinterpret_cast<uintptr_t>(out)) & 15u)
@@ -151,8 +174,8 @@ extern "C" PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const 
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int total = static_cast<int>(n_items);
-    build_static_work<<<(total + 127) / 128, 128, 0, s>>>(kv_indptr, last_page_len, batch, num_kv_heads, splits,
-                                                          page_size, tile, items, tasks, flags);
+    build_static_work<<<(total + 127) / 128, 128, 0, s>>>(kv_indptr, last_page_len, num_indices, batch, num_kv_heads,
+                                                          splits, page_size, tile, items, tasks, flags);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return report_cuda(e, "static work-list launch");
 
