@@ -666,6 +666,31 @@ def run_reference(args, rank, world):
     }
 
 
+SECONDARY_WORKLOADS = ("long_context_b1", "long_context_b4", "qwen15_mixed", "ragged", "prefill_chunk")
+SECONDARY_KEYS = ("value", "unit", "ms_per_step", "us_per_layer", "us_per_run_call", "pct_of_peak", "roofline",
+                  "e2e", "gpu_launches", "clocks", "steps", "warmup")
+
+
+def secondary_lines(args, rank, world, local) -> dict:
+    """The same measurement on the other workloads, each with its own timed region,
+    roofline and clock record (the headline line stays on the 128 x 301 step)."""
+    import copy
+    out = {}
+    for name in SECONDARY_WORKLOADS:
+        a = copy.copy(args)
+        a.workload = name
+        a.steps = max(1, min(args.steps, 300))
+        a.warmup = max(3, min(args.warmup, 10))
+        a.no_cpu_baseline = True
+        torch.cuda.empty_cache()
+        r = run_ours(a, rank, world, local)
+        line = {k: r[k] for k in SECONDARY_KEYS}
+        line["config"] = {k: r["config"][k] for k in ("workload", "description", "layers", "plan")}
+        out[name] = line
+    torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -689,6 +714,8 @@ def main(argv=None):
     ap.add_argument("--rope-theta", type=float, default=0.0,
                     help="> 0: rotary embedding of q and the appended K rows with this base")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the per-workload lines of the other workloads (default run, N = 1 only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -698,6 +725,8 @@ def main(argv=None):
         res = run_reference(args, rank, world)
     else:
         res = run_ours(args, rank, world, local)
+        if world == 1 and args.workload == "qwen05_decode" and not args.no_secondary:
+            res["secondary"] = secondary_lines(args, rank, world, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and torch.distributed.is_initialized():

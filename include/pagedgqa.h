@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define PGQA_ABI_VERSION 4
+#define PGQA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define PGQA_API __attribute__((visibility("default")))
@@ -128,10 +128,13 @@ typedef struct pgqa_plan_config {
                              kernel's resident CTAs per SM, at most 2 */
     int decode_kernel;    /* PGQA_DECODE_AUTO (tensor cores), PGQA_DECODE_TENSOR_CORE or
                              PGQA_DECODE_CUDA_CORE (fp32 FMA; kept as a measured alternative) */
-    int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3; 0 = chosen
-                             per plan_update: 3 when a whole slice fits in flight, or when a
-                             grid of long slices is less than one wave at two CTAs per SM and
-                             no prefill segment shares the call; else 2 */
+    int pipeline_stages;  /* tensor-core kernel: shared-memory stages per warp, 2 or 3, or 1 for
+                             the wide form (ten warps of one tile each, for slices of at most
+                             ten warp tiles and groups of up to 8 heads); 0 = chosen per
+                             plan_update: 1 when every slice fits the wide form, 3 when a
+                             whole slice fits in flight, or when a grid of long slices is
+                             less than one wave at two CTAs per SM and no prefill segment
+                             shares the call; else 2 */
     int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
     int decode_ctas;      /* tensor-core decode: 0 = one CTA per work item (the default);
                              n > 0 = n persistent CTAs walking the work list; -1 = one
@@ -144,6 +147,13 @@ typedef struct pgqa_plan_config {
                              generation tensor cores, S and O in tensor memory) or
                              PGQA_PREFILL_MMA_SYNC; PGQA_PREFILL_AUTO takes tcgen05, the
                              faster one on GB300 at every shape measured */
+    int test_stall_wait_us; /* 0 for normal use.  A test of the failure path, 1..1000000:
+                             in every CTA of the tensor-core decode kernel one warp
+                             withholds the copies of its first tile, waits that many
+                             microseconds for them, gives up, raises
+                             PGQA_FLAG_WAIT_TIMEOUT and ends with the CTA (whose output
+                             is then meaningless), instead of hanging.  Only that
+                             kernel's per-item schedule honours it. */
 } pgqa_plan_config;
 
 #define PGQA_PREFILL_AUTO 0
@@ -304,19 +314,31 @@ PGQA_API pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const v
 /*
  * pgqa_decode_static_scratch -- split-KV decode that allocates nothing.
  *
- * None of the pages has a counterpart to this call; it serves callers that
- * cannot allocate device memory: code running while a CUDA graph is being
- * captured (allocation would break the capture), runtimes that hand all device
- * memory to their own allocator, and embedded hosts without an allocator.  It
- * needs no plan: the slices are cut on the device from the device-side page
- * table, and the work list, merge list and split partials live in one 8 MiB
- * array inside the library (a static device array, held by every GPU that loads
- * the library until the process exits).  No cudaMalloc, cudaFree or allocating
- * library routine is called.
+ * None of the pages has a counterpart to this call.  It serves callers of this
+ * library that cannot allocate device memory: processes whose device memory is
+ * reserved up front and handed out by another allocator (a framework's caching
+ * allocator, an arena sized at start-up), where an allocation outside that
+ * reserve fails or fragments it; and embedded or real-time hosts that forbid
+ * allocation after initialisation, since cudaMalloc and cudaFree may block or
+ * synchronise the device at unpredictable times.  It needs no plan: the slices
+ * are cut on the device from the device-side page table, and the work list,
+ * merge list and split partials live in one 8 MiB array inside the library (a
+ * static device array, held by every GPU that loads the library until the
+ * process exits).  No cudaMalloc, cudaFree or allocating library routine is
+ * called.
  *
  *   q            [batch, num_qo_heads, head_dim]: one decode row per request
- *   k_pool/v_pool, kv_indices  as for pgqa_plan_update / pgqa_run
+ *   k_pool/v_pool  as for pgqa_run
  *   kv_indptr    [batch+1] int32, DEVICE
+ *   kv_indices   [num_indices] int32, DEVICE; may be NULL when num_indices is 0
+ *   num_indices  entries of kv_indices.  The table is checked on the device
+ *                where it is first read: a request whose page range
+ *                [kv_indptr[b], kv_indptr[b+1]) is negative, decreasing or
+ *                reaches past num_indices, or that has no pages but a non-zero
+ *                last_page_len, gets no keys (out = 0, lse = -inf) and raises
+ *                PGQA_FLAG_PAGE_INDEX; kv_indices is never read outside
+ *                [0, num_indices).  Page indices >= num_pages are skipped and
+ *                raise the same flag.
  *   last_page_len [batch] int32, DEVICE (values outside [1, page_size] for a
  *                request with pages are clamped and raise PGQA_FLAG_PAGE_INDEX)
  *   splits       slices per (request, kv head), 1..256 (1 = no merge)
@@ -325,15 +347,18 @@ PGQA_API pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const v
  * and fp32 partials); otherwise PGQA_ERR_CAPACITY and nothing is launched.
  * The first call on a device looks up the array's device address (once, with
  * that device current); make that first call before any stream capture.  All
- * calls share the array: calls whose kernels may overlap on the GPU (different
- * streams without ordering) race.  Nothing in the array needs to start zeroed.
+ * calls share the array, which keeps what the last call left in it: calls whose
+ * kernels may overlap on the GPU (different streams without ordering) race.
+ * Nothing in the array needs to start zeroed: each call writes its work list
+ * and partials before reading them.
  */
 PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const void *k_pool, const void *v_pool,
                                                 const int32_t *kv_indptr, const int32_t *kv_indices,
-                                                const int32_t *last_page_len, int batch, int64_t num_pages,
-                                                int page_size, int num_qo_heads, int num_kv_heads, int head_dim,
-                                                pgqa_dtype dtype, int splits, void *out, pgqa_dtype out_dtype,
-                                                float *lse, float sm_scale, pgqa_stream_t stream);
+                                                int64_t num_indices, const int32_t *last_page_len, int batch,
+                                                int64_t num_pages, int page_size, int num_qo_heads,
+                                                int num_kv_heads, int head_dim, pgqa_dtype dtype, int splits,
+                                                void *out, pgqa_dtype out_dtype, float *lse, float sm_scale,
+                                                pgqa_stream_t stream);
 
 /* Frees the plan's buffers (synchronising with its last enqueued copy).  NULL is a no-op. */
 PGQA_API pgqa_status pgqa_plan_destroy(pgqa_plan *plan);
@@ -421,7 +446,7 @@ typedef struct pgqa_schedule_info {
     int num_prefill_tiles;
     int split_tokens;       /* slice length chosen for the decode rows */
     int max_splits_used;    /* most slices any (row, kv head) got */
-    int pipeline_stages;    /* the tensor-core decode kernel's depth, 2 or 3 */
+    int pipeline_stages;    /* the tensor-core decode kernel's depth, 2 or 3; 1 = its wide form */
     int total_q_rows;
     int64_t kv_tokens;      /* sum of kv_len over requests */
 } pgqa_schedule_info;

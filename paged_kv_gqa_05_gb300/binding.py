@@ -48,7 +48,8 @@ class PlanConfig(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int), ("decode_kernel", ctypes.c_int),
                 ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
                 ("decode_ctas", ctypes.c_int), ("rope_max_position", ctypes.c_int),
-                ("rope_theta", ctypes.c_double), ("prefill_kernel", ctypes.c_int)]
+                ("rope_theta", ctypes.c_double), ("prefill_kernel", ctypes.c_int),
+                ("test_stall_wait_us", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -107,7 +108,8 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_append_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_float,
                                     ctypes.c_int, _vp]
     lib.pgqa_decode_static_scratch.restype = ctypes.c_int
-    lib.pgqa_decode_static_scratch.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int64,
+    lib.pgqa_decode_static_scratch.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_int64, _vp, ctypes.c_int,
+                                               ctypes.c_int64,
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                                ctypes.c_float, _vp]
@@ -121,7 +123,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_plan_schedule.argtypes = [ctypes.POINTER(PlanConfig), ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int,
                                        _i32p, ctypes.c_int64, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int,
                                        _vp, ctypes.c_int, ctypes.POINTER(ScheduleInfo)]
-    if lib.pgqa_abi_version() != 4:
+    if lib.pgqa_abi_version() != 5:
         raise RuntimeError("libpagedgqa.so ABI version mismatch")
     _lib = lib
     return lib
@@ -201,27 +203,30 @@ def kv_append_rope(plan: int, k_pool: torch.Tensor, v_pool: torch.Tensor, k: tor
 
 def _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits=0,
             split_tokens=0, ctas_per_sm=0, decode_kernel="auto", pipeline_stages=0, prefill_splits=0,
-            decode_ctas=0, rope_theta=0.0, rope_max_position=0, prefill_kernel="auto") -> PlanConfig:
+            decode_ctas=0, rope_theta=0.0, rope_max_position=0, prefill_kernel="auto",
+            test_stall_wait_us=0) -> PlanConfig:
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
     pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
     return PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                       max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
                       pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta),
-                      pf_kinds[prefill_kernel])
+                      pf_kinds[prefill_kernel], int(test_stall_wait_us))
 
 
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
                 pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0,
-                rope_theta: float = 0.0, rope_max_position: int = 0, prefill_kernel: str = "auto") -> int:
+                rope_theta: float = 0.0, rope_max_position: int = 0, prefill_kernel: str = "auto",
+                test_stall_wait_us: int = 0) -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
     decode_kernel: "auto" | "tensor_core" | "cuda_core"; rope_theta > 0 turns on the
     rotary embedding of q and the appended K rows (positions < rope_max_position);
-    prefill_kernel: "auto" | "tcgen05" | "mma_sync"."""
+    prefill_kernel: "auto" | "tcgen05" | "mma_sync"; test_stall_wait_us > 0 only in
+    the test of the bounded-wait failure path (see pgqa_plan_config)."""
     cfg = _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits,
                   split_tokens, ctas_per_sm, decode_kernel, pipeline_stages, prefill_splits, decode_ctas,
-                  rope_theta, rope_max_position, prefill_kernel)
+                  rope_theta, rope_max_position, prefill_kernel, test_stall_wait_us)
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value
@@ -291,8 +296,8 @@ def decode_static_scratch(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                           out_dtype: Optional[torch.dtype] = None, lse: Optional[torch.Tensor] = None,
                           sm_scale: float = 0.0, stream=None) -> torch.Tensor:
     """pgqa_decode_static_scratch: decode without any device allocation inside the
-    library (page table on the device).  `out` should be preallocated by callers
-    that cannot allocate."""
+    library (page table on the device; kv_indices may be empty).  Callers that
+    cannot allocate pass a preallocated `out`."""
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     for t, name in ((kv_indptr, "kv_indptr"), (kv_indices, "kv_indices"), (last_page_len, "last_page_len")):
@@ -301,7 +306,8 @@ def decode_static_scratch(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
     P, ps, Hkv, D = k_pool.shape
     _check(load().pgqa_decode_static_scratch(
         _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dev(kv_indptr, "kv_indptr"),
-        _dev(kv_indices, "kv_indices") if kv_indices.numel() else None, _dev(last_page_len, "last_page_len"),
+        _dev(kv_indices, "kv_indices") if kv_indices.numel() else None, kv_indices.numel(),
+        _dev(last_page_len, "last_page_len"),
         q.shape[0], P, ps, q.shape[1], Hkv, D, TORCH_TO_CODE[q.dtype], int(splits), _dev(out, "out"),
         TORCH_TO_CODE[out.dtype], None if lse is None else _dev(lse, "lse"), float(sm_scale), _stream(stream)))
     return out

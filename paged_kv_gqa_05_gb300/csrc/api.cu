@@ -170,7 +170,8 @@ struct pgqa_plan {
     int tile = 0;       // decode warp tile (tokens)
     int box_rows = 0;
     int ctas_per_sm = 0;     // CTA slots per SM for 2-stage plans (the most of any variant)
-    int slots_per_sm[4] = {0, 0, 0, 0};  // by pipeline depth (2 or 3): resident decode CTAs per SM
+    int slots_per_sm[4] = {0, 0, 0, 0};  // by pipeline depth (1 = the wide form, 2 or 3): resident decode
+                                         // CTAs per SM
     int kernel = PGQA_DECODE_TENSOR_CORE;
     int prefill_kind = PGQA_PREFILL_TCGEN05;  // prefill-segment kernel
     int prefill_pairs = 128;                  // (row, head) pairs per prefill tile of that kernel
@@ -368,8 +369,13 @@ static pgqa_status check_config(const pgqa_plan_config &c) {
         return fail(PGQA_ERR_INVALID_ARG, "prefill_kernel %d", c.prefill_kernel);
     if (c.prefill_splits < 0 || c.prefill_splits > 8)
         return fail(PGQA_ERR_INVALID_ARG, "prefill_splits %d (0..8)", c.prefill_splits);
-    if (c.pipeline_stages != 0 && c.pipeline_stages != 2 && c.pipeline_stages != 3)
-        return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 2 or 3)", c.pipeline_stages);
+    if (c.test_stall_wait_us < 0 || c.test_stall_wait_us > 1000000)
+        return fail(PGQA_ERR_INVALID_ARG, "test_stall_wait_us %d outside [0, 1000000]", c.test_stall_wait_us);
+    if (c.pipeline_stages < 0 || c.pipeline_stages > 3)
+        return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 1, 2 or 3)", c.pipeline_stages);
+    if (c.pipeline_stages == 1 && (c.decode_kernel == PGQA_DECODE_CUDA_CORE || c.decode_ctas != 0 || group > 8))
+        return fail(PGQA_ERR_UNSUPPORTED, "the wide decode form (pipeline_stages 1) runs groups of up to 8 heads "
+                    "on the per-item tensor-core kernel");
     if (c.rope_theta < 0.0 || std::isnan(c.rope_theta)) return fail(PGQA_ERR_INVALID_ARG, "rope_theta %g", c.rope_theta);
     if (c.rope_theta > 0.0) {
         if (c.rope_max_position < 1 || c.rope_max_position > (1 << 24))
@@ -387,7 +393,7 @@ static void plan_shape(pgqa_plan *p, const pgqa_plan_config &c) {
     p->tile = decode_warp_tile(c.head_dim);
     p->box_rows = std::min(c.page_size, p->tile);
     p->kernel = c.decode_kernel == PGQA_DECODE_CUDA_CORE ? PGQA_DECODE_CUDA_CORE : PGQA_DECODE_TENSOR_CORE;
-    p->stages = c.pipeline_stages == 3 ? 3 : 2;
+    p->stages = c.pipeline_stages == 0 ? 2 : c.pipeline_stages;
     // AUTO takes the tcgen05 kernel, measured faster on GB300 for 512-row causal chunks over
     // 1536 keys at every shape tried: d 64 g 7 19.5 against 26.1 us, d 64 g 4 (page 16) 25.8
     // against 36.4, d 128 g 6 25.5 against 28.1, d 128 g 16 39.4 against 60.0; beside a ragged
@@ -428,11 +434,11 @@ pgqa_status pgqa_plan_create(pgqa_plan **out, const pgqa_plan_config *cfg) {
     // two.  Timed on GB300, a third resident CTA adds no bandwidth once HBM is saturated
     // and only shortens every slice (uniform 4 x 32768-token batch, d 128: 304 slices
     // 26.3 us, 456 slices 28.8 us).
-    for (int st = 2; st <= 3 && e == cudaSuccess; ++st) {
+    for (int st = 1; st <= 3 && e == cudaSuccess; ++st) {
         int b = 2;  // the CUDA-core kernel's launch bound
         if (c.ctas_per_sm > 0) {
             b = c.ctas_per_sm;
-        } else if (p->kernel == PGQA_DECODE_TENSOR_CORE) {
+        } else if (p->kernel == PGQA_DECODE_TENSOR_CORE && (st > 1 || group <= 8)) {
             e = decode_blocks_per_sm(st, c.head_dim, group, c.dtype, &b);
             b = std::min(b, 2);
         }
@@ -520,7 +526,15 @@ static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any 
 // slower, 224-key slices (1 x 32k) lost 8 %, and a ragged call, whose decode rows then went
 // unsplit, 9 %.  Otherwise two, so that three CTAs fit on an SM and overlap each other's
 // set-up and epilogue.
+//
+// Slices of at most kDecodeWideWarps warp tiles take the wide form instead (reported as
+// depth 1): one warp per tile, the whole slice requested at once, so no warp of the CTA
+// runs more than one tile's chain of dependent steps.  On GB300 that chain, not the copy,
+// paced the 128 x 301 step: its busiest warps ran three tiles at ~0.55 us each.
 static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items, bool with_prefill) {
+    if (plan->kernel == PGQA_DECODE_TENSOR_CORE && plan->cfg.decode_ctas == 0 && plan->group <= 8 &&
+        max_slice <= static_cast<int64_t>(kDecodeWideWarps) * plan->tile)
+        return 1;
     const int64_t held = 3LL * kDecodeWarps * plan->tile;  // keys three stages hold
     if (max_slice <= held) return 3;
     if (!with_prefill && max_slice >= 2 * held &&
@@ -915,7 +929,7 @@ pgqa_status pgqa_plan_schedule(const pgqa_plan_config *cfg, int num_sms, const i
     if (!p) return fail(PGQA_ERR_CAPACITY, "out of host memory");
     plan_shape(p, *cfg);
     p->num_sms = num_sms;
-    p->slots_per_sm[2] = p->slots_per_sm[3] = cfg->ctas_per_sm > 0 ? cfg->ctas_per_sm : 2;
+    p->slots_per_sm[1] = p->slots_per_sm[2] = p->slots_per_sm[3] = cfg->ctas_per_sm > 0 ? cfg->ctas_per_sm : 2;
     Schedule sc;
     pgqa_status st = plan_capacity(p);
     if (st == PGQA_OK)
@@ -1056,6 +1070,7 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     // With a prefill grid just launched, the decode grid runs beside it.
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
     p.rope_cs = plan->rope_cs;
+    p.stall_wait_us = static_cast<uint32_t>(c.test_stall_wait_us);
     // The persistent schedule serves groups of up to 8 heads without RoPE; the rest run
     // one CTA per item.
     const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0 && plan->group <= 8 &&

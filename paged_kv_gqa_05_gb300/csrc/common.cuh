@@ -65,6 +65,9 @@ static_assert(sizeof(PrefillItem) == 48, "PrefillItem is 48 bytes");
 __host__ __device__ constexpr int decode_warp_tile(int head_dim) { return head_dim == 64 ? 32 : 16; }
 constexpr int kDecodeWarps = 4;
 constexpr int kDecodeStages = 3;
+// The wide form of the tensor-core decode kernel: this many warps, one stage each, for
+// slices of at most kDecodeWideWarps warp tiles (320 keys at head_dim 64, 160 at 128).
+constexpr int kDecodeWideWarps = 10;
 
 struct DecodeParams {
     const void *q;             // [rows, Hq, D]
@@ -95,6 +98,9 @@ struct DecodeParams {
                                // moves to the end (it only keeps completion order)
     const float2 *rope_cs;     // rotary (cos, sin) table [positions][D/2]; null: q and new rows
                                // are used as given
+    uint32_t stall_wait_us;    // test hook of the per-item tensor-core kernel (0 = off): warp 0
+                               // of every CTA withholds its first tile's copies and gives up
+                               // waiting for them after this many microseconds
 };
 
 struct PrefillParams {
@@ -212,15 +218,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the barrier phase with the given parity; gives up after ~2 s and
-// returns false (the caller raises PGQA_FLAG_WAIT_TIMEOUT instead of hanging).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Waits for the barrier phase with the given parity; gives up after about
+// limit_ns nanoseconds and returns false (the caller raises
+// PGQA_FLAG_WAIT_TIMEOUT instead of hanging).
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+        if ((it & 15u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The wait every pipeline barrier uses: ~2 s, far beyond any copy or product.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    return mbar_wait_limit(bar, parity, 2000000000ull);
 }
 
 // 3-D tiled TMA load into CTA shared memory, completion counted on `bar`.

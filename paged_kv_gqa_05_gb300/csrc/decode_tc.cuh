@@ -88,12 +88,12 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
 template <typename T>
 __device__ __forceinline__ float2 unpack2(uint32_t v) { return widen2<T>(v); }
 
-template <int D, int STAGES>
+template <int D, int STAGES, int WARPS = kDecodeWarps>
 struct TcCfg {
     static constexpr int TW = decode_warp_tile(D);      // tokens per warp tile (32 for d64, 16 for d128)
     static constexpr int MT = TW / 16;                   // token m-tiles per warp tile
     static constexpr int HALVES = D / 64;                // 128-byte (64-channel) column blocks per row
-    static constexpr int NW = kDecodeWarps;
+    static constexpr int NW = WARPS;
     static constexpr int ST = STAGES;
     static constexpr int HALF_BYTES = TW * 128;          // one 64-channel block of a tile
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
@@ -115,13 +115,17 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
     return (c >> 3) * (decode_warp_tile(D) * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-template <int D, int STAGES, int NH, bool ROPE, typename T>
-__global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 3 : 2)
+template <int D, int STAGES, int NH, bool ROPE, typename T, int NW = kDecodeWarps>
+__global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDecodeWarps) ? 3 : 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const DecodeParams p, int G) {
     // NH tiles of 8 query heads: G <= 8 * NH (NH = 2 serves groups of 9..16 heads).
     // ROPE: q and the new K rows turn by the plan's rotary table (p.rope_cs).
-    using C = TcCfg<D, STAGES>;
+    // NW warps with STAGES stages each: kDecodeWarps x 2 or 3 stages streams slices of
+    // any length; kDecodeWideWarps x 1 stage gives every warp of a short slice its own
+    // single tile, so the whole slice is in flight at once and the longest chain of
+    // dependent tile steps in the CTA is one tile long.
+    using C = TcCfg<D, STAGES, NW>;
     constexpr int HP = 8 * NH;  // heads padded to whole n tiles
     using M = MmaType<T>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
@@ -209,6 +213,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         }
     };
 
+    // Test hook (stall_wait_us != 0): warp 0 never issues its first tile, so nothing
+    // ever arrives on that stage's barrier and its first wait can only give up -- the
+    // path by which a CTA reports a stuck pipeline instead of hanging.  Nothing is in
+    // flight into that stage, and the other stages' copies are drained as usual.
+    const bool stall = p.stall_wait_us != 0 && warp == 0;
     // K/V loads start before the grid-dependency wait when the caller has stated
     // that nothing still in flight writes the pool rows this call reads.
     const int pre = my_tiles < C::ST ? my_tiles : C::ST;
@@ -216,16 +225,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         // Our predecessor is the prefill grid of the same call, which writes nothing
         // we read and started only after everything older completed.
         if (lane == 0)
-            for (int k = 0; k < pre; ++k) issue(k);
+            for (int k = stall ? 1 : 0; k < pre; ++k) issue(k);
     } else {
         if (p.prefetch_pool && lane == 0)
-            for (int k = 0; k < pre; ++k) issue(k);
+            for (int k = stall ? 1 : 0; k < pre; ++k) issue(k);
         pdl_wait();
         // Our predecessors are complete from here on, so a grid launched early after
         // this trigger never overlaps a kernel older than this one.
         pdl_launch_dependents();
         if (!p.prefetch_pool && lane == 0)
-            for (int k = 0; k < pre; ++k) issue(k);
+            for (int k = stall ? 1 : 0; k < pre; ++k) issue(k);
     }
 
     // Q^T fragments (B operand): b0 = q[head g8][16ks + 2c4, +1], b1 = same + 8.
@@ -333,7 +342,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
     for (int k = 0; k < my_tiles; ++k) {
         const int s = k % C::ST;
         // every lane observes the phase (TMA data visibility); the outcome is made warp-uniform
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar0 + 8 * s, (k / C::ST) & 1))) {
+        const bool landed = (stall && k == 0)
+                                ? mbar_wait_limit(bar0 + 8 * s, 0, uint64_t(p.stall_wait_us) * 1000u)
+                                : mbar_wait_bounded(bar0 + 8 * s, (k / C::ST) & 1);
+        if (!__all_sync(0xffffffffu, landed)) {
             if (lane == 0) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
             ok = false;
             break;
@@ -478,9 +490,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
         if (lane == 0 && k + C::ST < my_tiles) issue(k + C::ST);
     }
 
-    if (!ok && lane == 0) {
+    if (!ok && lane == 0) {  // copies still in flight land before the CTA's shared memory is reused
         const int issued = my_tiles < waited + C::ST ? my_tiles : waited + C::ST;
-        for (int k = waited; k < issued; ++k) mbar_wait_bounded(bar0 + 8 * (k % C::ST), (k / C::ST) & 1);
+        for (int k = waited; k < issued; ++k)
+            if (!(stall && k == 0)) mbar_wait_bounded(bar0 + 8 * (k % C::ST), (k / C::ST) & 1);
     }
 
     // ---- fused append: the item owning a query row stores that row's new K/V into the pool
@@ -608,7 +621,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (STAGES == 2 && NH == 1) ? 
 }
 
 // Raises the kernel's dynamic shared-memory limit once per device.
-template <int D, int STAGES, int NH, bool ROPE, typename T>
+template <int D, int STAGES, int NH, bool ROPE, typename T, int NW = kDecodeWarps>
 cudaError_t configure_decode_tc() {
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -616,19 +629,19 @@ cudaError_t configure_decode_tc() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, ROPE, T>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D, STAGES>::SMEM_BYTES);
+        e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, ROPE, T, NW>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D, STAGES, NW>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     return cudaSuccess;
 }
 
-template <int D, int STAGES, int NH, bool ROPE, typename T>
+template <int D, int STAGES, int NH, bool ROPE, typename T, int NW = kDecodeWarps>
 cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
                                 int num_items, bool pdl, cudaStream_t stream) {
-    using C = TcCfg<D, STAGES>;
-    cudaError_t e = configure_decode_tc<D, STAGES, NH, ROPE, T>();
+    using C = TcCfg<D, STAGES, NW>;
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, ROPE, T, NW>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
@@ -640,30 +653,33 @@ cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtens
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, ROPE, T>, tm_k, tm_v, p, group);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, ROPE, T, NW>, tm_k, tm_v, p, group);
 }
 
 // The rotary variant is a separate instantiation, so plans without RoPE run code
 // with no trace of it (timed: the runtime branch alone cost 3 % on 128 x 301).
-template <int D, int STAGES, int NH, typename T>
+template <int D, int STAGES, int NH, typename T, int NW = kDecodeWarps>
 cudaError_t launch_decode_tc_r(int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &p,
                                int num_items, bool pdl, cudaStream_t stream) {
-    return p.rope_cs != nullptr ? launch_decode_tc_st<D, STAGES, NH, true, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
-                                : launch_decode_tc_st<D, STAGES, NH, false, T>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    return p.rope_cs != nullptr
+               ? launch_decode_tc_st<D, STAGES, NH, true, T, NW>(group, tm_k, tm_v, p, num_items, pdl, stream)
+               : launch_decode_tc_st<D, STAGES, NH, false, T, NW>(group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 
 // CTAs of one per-item kernel variant resident on an SM at once (registers and
 // shared memory), the slot count of the split heuristic.
-template <int D, int STAGES, int NH, typename T>
+template <int D, int STAGES, int NH, typename T, int NW = kDecodeWarps>
 cudaError_t decode_tc_blocks_per_sm_st(int *blocks) {
-    cudaError_t e = configure_decode_tc<D, STAGES, NH, false, T>();
+    cudaError_t e = configure_decode_tc<D, STAGES, NH, false, T, NW>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_tc_kernel<D, STAGES, NH, false, T>,
-                                                         TcCfg<D, STAGES>::NW * 32, TcCfg<D, STAGES>::SMEM_BYTES);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, decode_tc_kernel<D, STAGES, NH, false, T, NW>,
+                                                         NW * 32, TcCfg<D, STAGES, NW>::SMEM_BYTES);
 }
 
+// stages 1 selects the wide form (kDecodeWideWarps warps, one tile each; groups of up to 8).
 template <int D, typename T>
 cudaError_t decode_tc_blocks_per_sm(int stages, int group, int *blocks) {
+    if (stages == 1) return decode_tc_blocks_per_sm_st<D, 1, 1, T, kDecodeWideWarps>(blocks);
     if (group > 8)
         return stages == 3 ? decode_tc_blocks_per_sm_st<D, 3, 2, T>(blocks) : decode_tc_blocks_per_sm_st<D, 2, 2, T>(blocks);
     return stages == 3 ? decode_tc_blocks_per_sm_st<D, 3, 1, T>(blocks) : decode_tc_blocks_per_sm_st<D, 2, 1, T>(blocks);
@@ -672,6 +688,10 @@ cudaError_t decode_tc_blocks_per_sm(int stages, int group, int *blocks) {
 template <int D, typename T>
 cudaError_t launch_decode_tc(int stages, int group, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                              const DecodeParams &p, int num_items, bool pdl, cudaStream_t stream) {
+    if (stages == 1) {
+        if (group > 8) return cudaErrorInvalidValue;  // the plan never picks the wide form for them
+        return launch_decode_tc_r<D, 1, 1, T, kDecodeWideWarps>(group, tm_k, tm_v, p, num_items, pdl, stream);
+    }
     if (group > 8)
         return stages == 3 ? launch_decode_tc_r<D, 3, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream)
                            : launch_decode_tc_r<D, 2, 2, T>(group, tm_k, tm_v, p, num_items, pdl, stream);

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.pgqa_abi_version() == 4
+    assert lib.pgqa_abi_version() == 5
     for code in range(7):
         assert lib.pgqa_status_string(code)
 

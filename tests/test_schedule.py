@@ -33,10 +33,13 @@ def check_schedule(w, sc, prefill_rows_on_tiles=True):
     assert info["num_items"] == len(slices) and info["num_merge_tasks"] == len(merges)
     assert info["num_prefill_tiles"] == len(tiles)
     assert info["total_q_rows"] == int(qo[-1]) and info["kv_tokens"] == int(kv_lens.sum())
-    assert info["pipeline_stages"] in (2, 3)
+    assert info["pipeline_stages"] in (1, 2, 3)
 
     # launch order: longest slices first
     lens = slices["key_end"] - slices["key_begin"]
+    if info["pipeline_stages"] == 1 and len(lens):
+        # the wide form: one warp tile per warp (ten warps) unless the caller forced it
+        assert G <= 8
     assert np.all(np.diff(lens) <= 0), "slices are not longest-first"
     assert np.all(slices["key_begin"] % tile == 0)
 
@@ -139,10 +142,19 @@ def test_workload_schedules(name):
 
 def test_short_rows_fill_one_wave_unsplit():
     """128 requests x 301 keys, 2 kv heads: 256 slices fit the 304 CTA slots of 152 SMs,
-    so no row is split, and every warp's tiles of a row fit three stages."""
+    so no row is split, and each row's ten 32-key tiles take the wide form (one warp each)."""
     sc = schedule(W.qwen05_decode())
     assert sc["info"]["num_items"] == 256 and sc["info"]["num_merge_tasks"] == 0
-    assert sc["info"]["pipeline_stages"] == 3
+    assert sc["info"]["pipeline_stages"] == 1
+    lens = sc["slices"]["key_end"] - sc["slices"]["key_begin"]
+    assert lens.max() <= 10 * 32
+
+
+def test_wide_form_only_for_short_slices_and_narrow_groups():
+    """Slices longer than ten warp tiles, and groups of more than 8 heads, keep the ring form."""
+    assert schedule(W.make("long_context_b4"))["info"]["pipeline_stages"] in (2, 3)
+    assert schedule(W.make("wide_group"))["info"]["pipeline_stages"] in (2, 3)
+    assert schedule(W.make("tiny"))["info"]["pipeline_stages"] == 1
 
 
 def test_long_row_is_spread_over_the_sms():
@@ -233,6 +245,11 @@ def test_table_errors_match_plan_update():
     with pytest.raises(B.PagedGQAError) as e:
         pg.plan_schedule(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, torch.bfloat16, num_sms=0, **base)
     assert e.value.name == "PGQA_ERR_INVALID_ARG"
+    for stall in (-1, 1000001):  # the failure-path test hook takes 0..1000000 microseconds
+        with pytest.raises(B.PagedGQAError) as e:
+            pg.plan_schedule(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, torch.bfloat16,
+                             test_stall_wait_us=stall, **base)
+        assert e.value.name == "PGQA_ERR_INVALID_ARG"
 
 
 def test_short_output_array_is_a_capacity_error():
