@@ -315,7 +315,11 @@ def run_ours(args, rank, world, local):
             elif with_append and L["slots"] is not None:
                 pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
                              stream=stream)
-            pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l], stream=stream)
+            # a step without new rows: no kernel in flight writes the pool rows the call reads,
+            # so its loads may begin before its dependency wait (the run-only graph keeps the
+            # plain call)
+            pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l],
+                   pool_stable=with_append and L["slots"] is None, stream=stream)
 
     with torch.cuda.stream(stream):
         update_plan()
@@ -399,7 +403,8 @@ def run_ours(args, rank, world, local):
                 elif L["slots"] is not None:
                     pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
                                  stream=stream)
-                pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l], stream=stream)
+                pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l],
+                       pool_stable=L["slots"] is None, stream=stream)
             if any(b == l + 1 for _, b in out_chunks):
                 ev_done[l + 1] = torch.cuda.Event()
                 ev_done[l + 1].record(stream)

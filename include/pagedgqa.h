@@ -293,7 +293,8 @@ PGQA_API pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool
  * which the page table must already cover (kv_len counts the new tokens).
  * Other arguments and the result are those of pgqa_run.
  *
- *   k_new, v_new  [total_q_rows, num_kv_heads, head_dim], the plan's dtype
+ *   k_new, v_new  [total_q_rows, num_kv_heads, head_dim], the plan's dtype; both NULL
+ *                 for a step without new rows (pgqa_run with `flags`)
  *   k_pool, v_pool  written (new rows only) and read
  *   flags         0, or PGQA_RUN_POOL_STABLE: no kernel still running when this
  *                 call's kernel starts writes any pool row this call reads
@@ -301,9 +302,10 @@ PGQA_API pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool
  *                 the kernel waits for its predecessor on the stream, hiding the
  *                 memory latency behind that kernel's tail.  A kernel that wrote
  *                 those rows and is the immediate predecessor voids the promise.
- * Errors: as pgqa_run; PGQA_ERR_UNSUPPORTED for a plan created with
- * PGQA_DECODE_CUDA_CORE; PGQA_ERR_INVALID_ARG when a request has more query
- * rows than keys.
+ * Errors: as pgqa_run; with new rows, PGQA_ERR_UNSUPPORTED for a plan created
+ * with PGQA_DECODE_CUDA_CORE and PGQA_ERR_INVALID_ARG when a request has more
+ * query rows than keys; PGQA_ERR_INVALID_ARG when only one of k_new, v_new is
+ * NULL.
  */
 #define PGQA_RUN_POOL_STABLE 1
 

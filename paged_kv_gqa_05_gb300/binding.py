@@ -250,14 +250,22 @@ def plan_update(plan: int, kv_indptr, last_page_len, kv_indices: torch.Tensor, n
 
 def run(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
         out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
-        lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, stream=None) -> torch.Tensor:
-    """pgqa_run; allocates `out` (torch) when it is not given."""
+        lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, pool_stable: bool = False,
+        stream=None) -> torch.Tensor:
+    """pgqa_run; allocates `out` (torch) when it is not given.  pool_stable: the
+    PGQA_RUN_POOL_STABLE promise (pgqa_append_run without new rows)."""
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
     if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
         raise ValueError("q and pools must share one dtype")
+    if pool_stable:
+        _check(load().pgqa_append_run(plan, None, None, _dev(q, "q"), _dev(k_pool, "k_pool"),
+                                      _dev(v_pool, "v_pool"), _dev(out, "out"), TORCH_TO_CODE[out.dtype],
+                                      None if lse is None else _dev(lse, "lse"), float(sm_scale), POOL_STABLE,
+                                      _stream(stream)))
+        return out
     _check(load().pgqa_run(plan, _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
                            _dev(out, "out"), TORCH_TO_CODE[out.dtype],
                            None if lse is None else _dev(lse, "lse"), float(sm_scale),

@@ -990,8 +990,6 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
             return fail(PGQA_ERR_INVALID_ARG, "a request has more query rows than keys: nothing to append them to");
         if (!aligned16(k_new) || !aligned16(v_new))
             return fail(PGQA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
-    } else if (flags & PGQA_RUN_POOL_STABLE) {
-        return fail(PGQA_ERR_INVALID_ARG, "PGQA_RUN_POOL_STABLE applies to pgqa_append_run");
     }
     if (plan->n_items == 0 && plan->n_prefill == 0) return PGQA_OK;
     if (!q || !k_pool || !v_pool || !out) return fail(PGQA_ERR_INVALID_ARG, "NULL tensor");
@@ -1037,7 +1035,7 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
         pp.v_new = v_new;
         pp.k_pool = k_pool;
         pp.v_pool = v_pool;
-        pp.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
+        pp.prefetch_pool = (flags & PGQA_RUN_POOL_STABLE) ? 1 : 0;
         pp.partial_o = plan->d_partial_o;
         pp.partial_lse = plan->d_partial_lse;
         pp.rope_cs = plan->rope_cs;
@@ -1066,7 +1064,7 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.k_pool = k_pool;
     p.v_pool = v_pool;
     p.num_kv_heads = c.num_kv_heads;
-    p.prefetch_pool = (fused && (flags & PGQA_RUN_POOL_STABLE)) ? 1 : 0;
+    p.prefetch_pool = (flags & PGQA_RUN_POOL_STABLE) ? 1 : 0;
     // With a prefill grid just launched, the decode grid runs beside it.
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
     p.rope_cs = plan->rope_cs;
@@ -1107,7 +1105,8 @@ pgqa_status pgqa_run(pgqa_plan *plan, const void *q, const void *k_pool, const v
 pgqa_status pgqa_append_run(pgqa_plan *plan, const void *k_new, const void *v_new, const void *q, void *k_pool,
                             void *v_pool, void *out, pgqa_dtype out_dtype, float *lse, float sm_scale, int flags,
                             pgqa_stream_t stream) {
-    if (!k_new || !v_new) return fail(PGQA_ERR_INVALID_ARG, "k_new / v_new is NULL");
+    // both NULL: no new rows, a run() that honours the flags
+    if (!k_new != !v_new) return fail(PGQA_ERR_INVALID_ARG, "k_new and v_new go together");
     return run_impl(plan, k_new, v_new, q, k_pool, v_pool, out, out_dtype, lse, sm_scale, flags, stream);
 }
 

@@ -66,6 +66,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
     pdl_wait();
 
+    // The partial outputs do not depend on the weights: the first kPrefetch of this
+    // thread's slices are requested together with the lse values, so the block waits
+    // out one memory latency instead of two.
+    const int c4 = threadIdx.x & 7, sg = threadIdx.x >> 3;
+    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + c0 + c4 * 4;
+    const size_t stride = static_cast<size_t>(G) * D;
+    constexpr int kPrefetch = 8;  // slices sg + 32 i, i < kPrefetch: lists of up to 256 slices
+    float4 pre[kPrefetch];
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+        const int s = sg + 32 * i;
+        pre[i] = s < ns ? __ldg(reinterpret_cast<const float4 *>(base + s * stride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
     const float *lse_in = p.partial_lse + static_cast<size_t>(t.slot_base) * G + h;
     float mx = -INFINITY;
     for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
@@ -82,12 +96,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
     sum = block_reduce(sum, scratch, false);  // also publishes w[] to the block
 
-    const int c4 = threadIdx.x & 7, sg = threadIdx.x >> 3;
-    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + c0 + c4 * 4;
-    const size_t stride = static_cast<size_t>(G) * D;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+        const int s = sg + 32 * i;
+        const float ws = s < ns ? w[s] : 0.f;
+        if (ws != 0.f) {  // also taken for NaN weights
+            acc.x += ws * pre[i].x;
+            acc.y += ws * pre[i].y;
+            acc.z += ws * pre[i].z;
+            acc.w += ws * pre[i].w;
+        }
+    }
 #pragma unroll 4
-    for (int s = sg; s < ns; s += 32) {
+    for (int s = sg + 32 * kPrefetch; s < ns; s += 32) {
         const float ws = w[s];
         if (ws != 0.f) {  // also taken for NaN weights
             const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
@@ -128,6 +150,25 @@ __global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, in
 
     pdl_wait();
 
+    // Partial outputs of the first kPrefetch slices are requested with the lse values
+    // (they do not depend on the weights): one memory latency before the fold, not two.
+    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + lane * V;
+    const size_t stride = static_cast<size_t>(G) * D;
+    constexpr int kPrefetch = 8;
+    float pre[kPrefetch][V];
+#pragma unroll
+    for (int s = 0; s < kPrefetch; ++s) {
+        if (s < ns) {
+            if (V == 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
+                pre[s][0] = v.x; pre[s][1 % V] = v.y; pre[s][2 % V] = v.z; pre[s][3 % V] = v.w;
+            } else {
+                const float2 v = __ldg(reinterpret_cast<const float2 *>(base + s * stride));
+                pre[s][0] = v.x; pre[s][1 % V] = v.y;
+            }
+        }
+    }
+
     const float l = lane < ns ? p.partial_lse[static_cast<size_t>(t.slot_base + lane) * G + h] : -INFINITY;
     float mx = l;
 #pragma unroll
@@ -137,13 +178,19 @@ __global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, in
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
 
-    const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + lane * V;
-    const size_t stride = static_cast<size_t>(G) * D;
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kPrefetch; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);  // lanes >= ns carry weight 0
+        if (s < ns) {
+#pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] += ws * pre[s][j];
+        }
+    }
 #pragma unroll 8
-    for (int s = 0; s < ns; ++s) {
+    for (int s = kPrefetch; s < ns; ++s) {
         const float ws = __shfl_sync(0xffffffffu, w, s);
         if (V == 4) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(base + s * stride));
