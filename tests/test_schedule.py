@@ -313,3 +313,12 @@ def test_checker_catches_broken_schedules(mistake):
     check_schedule(w, sc)
     with pytest.raises(AssertionError):
         check_schedule(w, _mutants(sc)[mistake])
+
+
+def test_prefill_slices_leave_room_for_decode_rows():
+    """A chunk alone takes up to two prefill CTAs per SM; beside decode rows about one, so
+    that decode CTAs run next to the prefill tiles instead of waiting for them."""
+    alone = schedule(W.make("prefill_chunk"))["info"]
+    mixed = schedule(W.make("ragged"))["info"]
+    assert SMS < alone["num_prefill_tiles"] <= 2 * SMS
+    assert mixed["num_items"] > 0 and mixed["num_prefill_tiles"] <= SMS
