@@ -1,5 +1,6 @@
 """GPU: the benchmark's timed step in the launch configuration it times -- every
-layer's call with the default plan options (fused append where the workload appends),
+layer's call with the default plan options (fused append where the workload appends;
+without new rows, a run() that may load the pools before its dependency wait),
 16-bit outputs, all layers replayed from one CUDA graph after a plan update -- checked
 against the CPU oracle on layer 0, whose inputs come from the CPU generator."""
 import os
@@ -18,7 +19,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("name", ["qwen05_decode", "qwen15_mixed", "long_context_b4", "ragged", "prefill_chunk"])
+@pytest.mark.parametrize("name", ["qwen05_decode", "qwen15_mixed", "long_context_b1", "long_context_b4", "ragged",
+                                  "prefill_chunk"])
 def test_benchmark_step(name):
     sys.path.insert(0, ROOT)
     import bench
@@ -42,9 +44,9 @@ def test_benchmark_step(name):
                 if L["slots"] is not None:
                     pg.append_run(plan.handle, L["k_new"][l], L["v_new"][l], L["q"][l], L["k_pool"][l],
                                   L["v_pool"][l], out=L["out"][l], pool_stable=True, stream=stream)
-                else:
+                else:  # no new rows: a run() under the same promise, as the benchmark's step
                     pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l],
-                           stream=stream)
+                           pool_stable=True, stream=stream)
 
         with torch.cuda.stream(stream):
             update()

@@ -136,3 +136,27 @@ def test_split_rows_repeated_calls(kernel_opts):
             torch.cuda.synchronize()
             H.compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, f"splits {kernel_opts} graph")
     assert pg.read_device_flags() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen15_mixed", "long_context_b1", "ragged"])
+def test_pool_stable_run_is_the_plain_run(name):
+    """pgqa_append_run without new rows and with PGQA_RUN_POOL_STABLE (the loads may start
+    before the dependency wait) gives the plain run()'s result bit for bit, and the oracle's."""
+    import paged_kv_gqa_05_gb300 as pg
+    w, (ro, rl) = _ref(name)
+    dev = H.to_device(w)
+    if w.k_new is not None:
+        pg.kv_append(dev["k_pool"], dev["v_pool"], dev["k_new"], dev["v_new"], dev["slot_mapping"])
+    with pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dev["q"].dtype,
+                 max_batch=w.batch, max_q_rows=w.rows) as plan:
+        plan.update(w.kv_indptr, w.last_page_len, dev["kv_indices"], w.num_pages, qo_indptr=w.qo_indptr,
+                    causal=w.causal)
+        res = []
+        for stable in (False, True):
+            out = torch.full(dev["q"].shape, float("nan"), dtype=torch.float32, device="cuda")
+            lse = torch.full(dev["q"].shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+            plan.run(dev["q"], dev["k_pool"], dev["v_pool"], out=out, lse=lse, pool_stable=stable)
+            torch.cuda.synchronize()
+            res.append((out.double().cpu().numpy(), lse.double().cpu().numpy()))
+    assert np.array_equal(res[0][0], res[1][0]) and np.array_equal(res[0][1], res[1][1])
+    H.compare(res[1][0], res[1][1], ro, rl, name + "/pool-stable run")
