@@ -25,8 +25,7 @@
  *   - Query head h reads KV head h / (num_qo_heads / num_kv_heads).
  *   - Supported shapes: head_dim 64 or 128; page_size 16, 32, 64, 128 or 256;
  *     num_qo_heads / num_kv_heads between 1 and 16 (1 and 8 for the CUDA-core
- *     decode kernel, the persistent decode schedule and
- *     pgqa_decode_static_scratch); bf16 or fp16 q/k/v.
+ *     decode kernel and pgqa_decode_static_scratch); bf16 or fp16 q/k/v.
  *     Anything else returns PGQA_ERR_UNSUPPORTED.
  *   - Pool, q, k, v and out pointers must be 16-byte aligned.
  */
@@ -136,10 +135,6 @@ typedef struct pgqa_plan_config {
                              less than one wave at two CTAs per SM and no prefill segment
                              shares the call; else 2 */
     int prefill_splits;   /* key slices per prefill tile (1..8); 0 = as many as fit one wave */
-    int decode_ctas;      /* tensor-core decode: 0 = one CTA per work item (the default);
-                             n > 0 = n persistent CTAs walking the work list; -1 = one
-                             persistent CTA per SM.  Groups wider than 8 heads always run
-                             one CTA per item. */
     int rope_max_position; /* RoPE plans: positions 0 .. rope_max_position - 1 are valid */
     double rope_theta;    /* > 0: rotary position embedding with this base (see below);
                              0: none */

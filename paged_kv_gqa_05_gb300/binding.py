@@ -47,7 +47,7 @@ class PlanConfig(ctypes.Structure):
                 ("max_splits", ctypes.c_int), ("split_tokens", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int), ("decode_kernel", ctypes.c_int),
                 ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
-                ("decode_ctas", ctypes.c_int), ("rope_max_position", ctypes.c_int),
+                ("rope_max_position", ctypes.c_int),
                 ("rope_theta", ctypes.c_double), ("prefill_kernel", ctypes.c_int),
                 ("test_stall_wait_us", ctypes.c_int)]
 
@@ -203,20 +203,20 @@ def kv_append_rope(plan: int, k_pool: torch.Tensor, v_pool: torch.Tensor, k: tor
 
 def _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits=0,
             split_tokens=0, ctas_per_sm=0, decode_kernel="auto", pipeline_stages=0, prefill_splits=0,
-            decode_ctas=0, rope_theta=0.0, rope_max_position=0, prefill_kernel="auto",
+            rope_theta=0.0, rope_max_position=0, prefill_kernel="auto",
             test_stall_wait_us=0) -> PlanConfig:
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
     pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
     return PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                       max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
-                      pipeline_stages, prefill_splits, decode_ctas, rope_max_position, float(rope_theta),
+                      pipeline_stages, prefill_splits, rope_max_position, float(rope_theta),
                       pf_kinds[prefill_kernel], int(test_stall_wait_us))
 
 
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                 dtype: torch.dtype, max_batch: int, max_q_rows: int, max_splits: int = 0,
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
-                pipeline_stages: int = 0, prefill_splits: int = 0, decode_ctas: int = 0,
+                pipeline_stages: int = 0, prefill_splits: int = 0,
                 rope_theta: float = 0.0, rope_max_position: int = 0, prefill_kernel: str = "auto",
                 test_stall_wait_us: int = 0) -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
@@ -225,7 +225,7 @@ def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: 
     prefill_kernel: "auto" | "tcgen05" | "mma_sync"; test_stall_wait_us > 0 only in
     the test of the bounded-wait failure path (see pgqa_plan_config)."""
     cfg = _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits,
-                  split_tokens, ctas_per_sm, decode_kernel, pipeline_stages, prefill_splits, decode_ctas,
+                  split_tokens, ctas_per_sm, decode_kernel, pipeline_stages, prefill_splits,
                   rope_theta, rope_max_position, prefill_kernel, test_stall_wait_us)
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))

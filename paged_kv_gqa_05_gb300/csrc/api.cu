@@ -17,18 +17,18 @@
 
 namespace pgqa {
 using DecodeLauncher = cudaError_t (*)(int, int, int, const CUtensorMap &, const CUtensorMap &,
-                                        const DecodeParams &, int, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
-cudaError_t launch_decode_bf16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
-cudaError_t launch_decode_fp16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, int, bool, cudaStream_t);
+                                        const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_bf16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d64(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
+cudaError_t launch_decode_fp16_d128(int, int, int, const CUtensorMap &, const CUtensorMap &, const DecodeParams &, int, bool, cudaStream_t);
 
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, int grid, bool pdl,
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
                           cudaStream_t stream) {
     DecodeLauncher f = dtype == PGQA_BF16 ? (head_dim == 64 ? launch_decode_bf16_d64 : launch_decode_bf16_d128)
                                           : (head_dim == 64 ? launch_decode_fp16_d64 : launch_decode_fp16_d128);
-    return f(kind, stages, group, tm_k, tm_v, p, num_items, grid, pdl, stream);
+    return f(kind, stages, group, tm_k, tm_v, p, num_items, pdl, stream);
 }
 cudaError_t decode_blocks_per_sm_bf16_d64(int, int, int *);
 cudaError_t decode_blocks_per_sm_bf16_d128(int, int, int *);
@@ -364,7 +364,6 @@ static pgqa_status check_config(const pgqa_plan_config &c) {
         return fail(PGQA_ERR_INVALID_ARG, "negative plan option");
     if (c.decode_kernel < PGQA_DECODE_AUTO || c.decode_kernel > PGQA_DECODE_CUDA_CORE)
         return fail(PGQA_ERR_INVALID_ARG, "decode_kernel %d", c.decode_kernel);
-    if (c.decode_ctas < -1) return fail(PGQA_ERR_INVALID_ARG, "decode_ctas %d", c.decode_ctas);
     if (c.prefill_kernel < PGQA_PREFILL_AUTO || c.prefill_kernel > PGQA_PREFILL_MMA_SYNC)
         return fail(PGQA_ERR_INVALID_ARG, "prefill_kernel %d", c.prefill_kernel);
     if (c.prefill_splits < 0 || c.prefill_splits > 8)
@@ -373,7 +372,7 @@ static pgqa_status check_config(const pgqa_plan_config &c) {
         return fail(PGQA_ERR_INVALID_ARG, "test_stall_wait_us %d outside [0, 1000000]", c.test_stall_wait_us);
     if (c.pipeline_stages < 0 || c.pipeline_stages > 3)
         return fail(PGQA_ERR_UNSUPPORTED, "pipeline_stages %d (0, 1, 2 or 3)", c.pipeline_stages);
-    if (c.pipeline_stages == 1 && (c.decode_kernel == PGQA_DECODE_CUDA_CORE || c.decode_ctas != 0 || group > 8))
+    if (c.pipeline_stages == 1 && (c.decode_kernel == PGQA_DECODE_CUDA_CORE || group > 8))
         return fail(PGQA_ERR_UNSUPPORTED, "the wide decode form (pipeline_stages 1) runs groups of up to 8 heads "
                     "on the per-item tensor-core kernel");
     if (c.rope_theta < 0.0 || std::isnan(c.rope_theta)) return fail(PGQA_ERR_INVALID_ARG, "rope_theta %g", c.rope_theta);
@@ -532,7 +531,7 @@ static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any 
 // runs more than one tile's chain of dependent steps.  On GB300 that chain, not the copy,
 // paced the 128 x 301 step: its busiest warps ran three tiles at ~0.55 us each.
 static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items, bool with_prefill) {
-    if (plan->kernel == PGQA_DECODE_TENSOR_CORE && plan->cfg.decode_ctas == 0 && plan->group <= 8 &&
+    if (plan->kernel == PGQA_DECODE_TENSOR_CORE && plan->group <= 8 &&
         max_slice <= static_cast<int64_t>(kDecodeWideWarps) * plan->tile)
         return 1;
     const int64_t held = 3LL * kDecodeWarps * plan->tile;  // keys three stages hold
@@ -1075,14 +1074,8 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
     p.rope_cs = plan->rope_cs;
     p.stall_wait_us = static_cast<uint32_t>(c.test_stall_wait_us);
-    // The persistent schedule serves groups of up to 8 heads without RoPE; the rest run
-    // one CTA per item.
-    const int grid = (plan->kernel == PGQA_DECODE_TENSOR_CORE && c.decode_ctas != 0 && plan->group <= 8 &&
-                      plan->rope_cs == nullptr)
-                         ? (c.decode_ctas > 0 ? c.decode_ctas : plan->num_sms)
-                         : 0;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,
-                      grid, true, st);
+                      true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     }
     if (plan->n_tasks > 0) {

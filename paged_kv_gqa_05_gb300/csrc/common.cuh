@@ -140,12 +140,10 @@ struct MergeParams {
     int head_dim;
 };
 
-// Launchers (defined in the kernel translation units).
-// grid > 0: persistent tensor-core kernel with that many CTAs walking the work list;
-// grid <= 0: one CTA per work item.
+// Launchers (defined in the kernel translation units).  Decode: one CTA per work item.
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, int grid,
-                          bool pdl, cudaStream_t stream);
+                          const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
+                          cudaStream_t stream);
 cudaError_t launch_prefill(int kind, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                            const CUtensorMap &tm_v, const PrefillParams &p, int num_items, bool pdl,
                            cudaStream_t stream);

@@ -197,7 +197,7 @@ extern "C" PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const 
     p.num_kv_heads = num_kv_heads;
     // The work list was just written by a kernel: launch without programmatic
     // overlap so the decode kernel starts only after it is complete.
-    e = launch_decode(PGQA_DECODE_TENSOR_CORE, 2, head_dim, group, dtype, mk, mv, p, total, 0, false, s);
+    e = launch_decode(PGQA_DECODE_TENSOR_CORE, 2, head_dim, group, dtype, mk, mv, p, total, false, s);
     if (e != cudaSuccess) return report_cuda(e, "decode launch");
     if (splits > 1) {
         MergeParams mp{};

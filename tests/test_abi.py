@@ -67,11 +67,11 @@ def test_argument_checks_before_device(lib):
     assert lib.pgqa_run(None, None, None, None, None, 0, None, 0.0, None) == 1
     # RoPE configuration checks, also before any device call
     PC = __import__("paged_kv_gqa_05_gb300").binding.PlanConfig
-    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0,
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0,
                                                                   4096, -1.0))) == 1  # negative theta
-    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0, 0,
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 0, 0, 0,
                                                                   0, 1.0e6))) == 1  # no positions
-    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 2, 0, 0, 0,
+    assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 2, 0, 0,
                                                                   4096, 1.0e6))) == 2  # CUDA-core kernel
     assert lib.pgqa_kv_append_rope(None, None, None, 1, None, None, None, None, 1, None) == 1
 
@@ -80,9 +80,9 @@ def test_plan_config_layout():
     """The ctypes mirror of pgqa_plan_config: natural C alignment, rope_theta last."""
     from paged_kv_gqa_05_gb300 import binding
     PC = binding.PlanConfig
-    assert PC.max_q_rows.offset == 24 and PC.decode_ctas.offset == 56
-    assert PC.rope_max_position.offset == 60 and PC.rope_theta.offset == 64
-    assert PC.prefill_kernel.offset == 72 and ctypes.sizeof(PC) == 80
+    assert PC.max_q_rows.offset == 24 and PC.prefill_splits.offset == 52
+    assert PC.rope_max_position.offset == 56 and PC.rope_theta.offset == 64
+    assert PC.prefill_kernel.offset == 72 and PC.test_stall_wait_us.offset == 76 and ctypes.sizeof(PC) == 80
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -36,8 +36,8 @@ def check_pool(w, dev):
     assert np.array_equal(W.raw16(dev["v_pool"]), vp), "fused append V rows differ"
 
 
-@pytest.mark.parametrize("opts", [{}, {"split_tokens": 64}, {"max_splits": 1}, {"decode_ctas": 3},
-                                  {"decode_ctas": -1}])
+@pytest.mark.parametrize("opts", [{}, {"split_tokens": 64}, {"max_splits": 1}, {"pipeline_stages": 1},
+                                  {"pipeline_stages": 2}])
 @pytest.mark.parametrize("pool_stable", [False, True])
 def test_fused_decode_step(opts, pool_stable):
     w = W.qwen05_decode(batch=32, cached=300, num_pages=1024)

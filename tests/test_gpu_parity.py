@@ -100,8 +100,8 @@ def test_sampled_rows_full_size_long_context_b4():
     assert info["num_merge_tasks"] > 0
 
 
-@pytest.mark.parametrize("kernel_opts", [{}, {"decode_ctas": -1}, {"decode_kernel": "cuda_core"}],
-                         ids=["per-item", "persistent", "cuda-core"])
+@pytest.mark.parametrize("kernel_opts", [{}, {"pipeline_stages": 2}, {"decode_kernel": "cuda_core"}],
+                         ids=["per-item", "two-stage", "cuda-core"])
 def test_split_rows_repeated_calls(kernel_opts):
     """128-token slices (6 to 24 per row) on each decode kernel, merged by the merge
     kernel.  The same plan runs three times eagerly and twice from a CUDA graph, each

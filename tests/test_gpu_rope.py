@@ -105,11 +105,11 @@ def check_fused(w: W.Workload, what: str, **opts):
     assert same(gk, kp) and same(gv, vp), what + ": rows other than the new ones changed"
 
 
-@pytest.mark.parametrize("opts", [{}, {"split_tokens": 64}, {"decode_ctas": -1}])
+@pytest.mark.parametrize("opts", [{}, {"split_tokens": 64}, {"pipeline_stages": 3}])
 @pytest.mark.parametrize("pool_stable", [False, True])
 def test_rope_decode_step(opts, pool_stable):
     """The 128 x 300-style decode step (smaller batch) with RoPE; forced splits put the
-    new row in the last slice of several; a persistent request runs one CTA per item."""
+    new row in the last slice of several; the 3-stage ring form as well as the plan's choice."""
     w = W.qwen05_decode(batch=32, cached=300, num_pages=1024)
     check_fused(w, f"rope decode {opts} stable={pool_stable}", pool_stable=pool_stable, **opts)
 

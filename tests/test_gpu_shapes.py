@@ -17,9 +17,10 @@ LENS = [0, 1, 5, 16, 17, 31, 33, 100, 257, 700]
 
 
 KERNELS = ["tensor_core", "cuda_core"]
-# tensor-core decode schedules: persistent (one CTA per SM), a tiny persistent grid (many
-# items per CTA), and one CTA per work item
-SCHEDULES = {"per_item": {}, "grid3": {"decode_ctas": 3}, "persistent": {"decode_ctas": -1}}
+# tensor-core decode forms: the plan's choice, the wide form (one tile per warp; with
+# forced 32-key slices or longer rows it loops on its single stage), and the 2- and 3-stage rings
+SCHEDULES = {"auto": {}, "wide": {"pipeline_stages": 1}, "ring2": {"pipeline_stages": 2},
+             "ring3": {"pipeline_stages": 3}}
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -67,13 +68,12 @@ def test_wide_groups(group, dtype, head_dim, stages):
     H.compare(out, lse, ro, rl, f"wide g{group}/{dtype}/d{head_dim}/st{stages}")
 
 
-@pytest.mark.parametrize("decode_ctas", [-1, 3])
-def test_wide_group_persistent_request_runs_per_item(decode_ctas):
-    """A persistent schedule asked for with a 16-head group runs one CTA per item."""
-    w = W.custom("wgp", [17, 300, 64], 32, 16, 1, 128, "bf16", 32, seed=3)
-    ro, rl = H.oracle_outputs(w)
-    out, lse, _ = H.gpu_outputs(w, split_tokens=64, decode_ctas=decode_ctas)
-    H.compare(out, lse, ro, rl, f"wide persistent {decode_ctas}")
+def test_wide_form_is_refused_for_wide_groups():
+    """The wide decode form serves groups of up to 8 heads; asked for with 16 it is refused."""
+    import paged_kv_gqa_05_gb300 as pg
+    with pytest.raises(pg.PagedGQAError) as e:
+        pg.Plan(32, 2, 128, 16, torch.bfloat16, max_batch=1, max_q_rows=1, pipeline_stages=1)
+    assert e.value.name == "PGQA_ERR_UNSUPPORTED"
 
 
 def test_all_empty_batch():
