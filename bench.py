@@ -243,18 +243,23 @@ def build_layers(name: str, layers: int, seed: int, device: torch.device):
     inputs = torch.empty(layers * per_layer, dtype=dt, device=device)
     gen = torch.Generator(device=device).manual_seed(seed * 1000 + 999)
     inputs.copy_(torch.randn(inputs.shape, generator=gen, device=device).to(dt))
-    q, kn, vn = [], [], []
-    for l in range(layers):
-        base = l * per_layer
-        q.append(inputs[base:base + q_elems].view(rows, Hq, D))
-        kn.append(inputs[base + q_elems:base + q_elems + kv_elems].view(T, Hkv, D))
-        vn.append(inputs[base + q_elems + kv_elems:base + per_layer].view(T, Hkv, D))
+    def views(buf):
+        """Per-layer q, k_new, v_new views of one step's input buffer."""
+        q, kn, vn = [], [], []
+        for l in range(layers):
+            base = l * per_layer
+            q.append(buf[base:base + q_elems].view(rows, Hq, D))
+            kn.append(buf[base + q_elems:base + q_elems + kv_elems].view(T, Hkv, D))
+            vn.append(buf[base + q_elems + kv_elems:base + per_layer].view(T, Hkv, D))
+        return q, kn, vn
+
+    q, kn, vn = views(inputs)
     q[0].copy_(w.q.to(device))
     if T:
         kn[0].copy_(w.k_new.to(device))
         vn[0].copy_(w.v_new.to(device))
     out = torch.empty(layers, rows, Hq, D, dtype=dt, device=device)
-    return dict(w=w, k_pool=kp, v_pool=vp, q=q, k_new=kn, v_new=vn, inputs=inputs, out=out,
+    return dict(w=w, k_pool=kp, v_pool=vp, q=q, k_new=kn, v_new=vn, inputs=inputs, out=out, views=views,
                 kv_indices=torch.from_numpy(w.kv_indices).to(device),
                 slots=None if w.slot_mapping is None else torch.from_numpy(w.slot_mapping).to(device))
 
@@ -287,7 +292,7 @@ def run_ours(args, rank, world, local):
     plan = pg.Plan(w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, dt, max_batch=w.batch,
                    max_q_rows=w.rows, max_splits=args.max_splits, split_tokens=args.split_tokens,
                    ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel,
-                   pipeline_stages=args.stages, decode_ctas=args.decode_ctas,
+                   pipeline_stages=args.stages,
                    rope_theta=args.rope_theta, rope_max_position=int(w.kv_lens.max()) if args.rope_theta > 0 else 0,
                    prefill_kernel=args.prefill_kernel, prefill_splits=args.prefill_splits)
     stream = torch.cuda.Stream(device)
@@ -349,88 +354,67 @@ def run_ours(args, rank, world, local):
         replay("step")
 
     # e2e: pinned host copies of every step's inputs in and outputs out.  With graphs the
-    # copies are pipelined with the layers: layer l's inputs go up on one copy stream and
-    # layer l waits only for them; its output comes down on another as soon as it is done.
+    # steps are double-buffered, as a serving loop runs them: while step s computes on one
+    # set of device buffers, step s + 1's inputs go up into the other set on one copy stream
+    # and step s - 1's outputs come down from it on another.  The timed region holds K steps
+    # plus the first step's upload and the last step's download: K + 1 copies each way.
     host_in = torch.empty(L["inputs"].shape, dtype=dt, pin_memory=True)
     host_in.copy_(L["inputs"])
     host_out = torch.empty(L["out"].shape, dtype=dt, pin_memory=True)
-    per_layer_in = L["inputs"].numel() // layers
-
     h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    inputs2, out2 = torch.empty_like(L["inputs"]), torch.empty_like(L["out"])
+    bufsets = [(L["inputs"], L["q"], L["k_new"], L["v_new"], L["out"]), (inputs2, *L["views"](inputs2), out2)]
 
-    def chunks(n, first_sizes):
-        """[a, b) layer ranges: the given sizes first, then doubling, to n."""
-        out, a, size = [], 0, 1
-        for sz in first_sizes:
-            if a >= n:
-                break
-            out.append((a, min(n, a + sz)))
-            a, size = out[-1][1], sz
-        while a < n:
-            size *= 2
-            out.append((a, min(n, a + size)))
-            a = out[-1][1]
-        return out
+    def layers_on(bs):
+        _, qs, kns, vns, outs = bs
+        for l in range(layers):
+            if fused:
+                pg.append_run(plan.handle, kns[l], vns[l], qs[l], L["k_pool"][l], L["v_pool"][l], out=outs[l],
+                              pool_stable=True, stream=stream)
+                continue
+            if L["slots"] is not None and positions is not None:
+                plan.kv_append_rope(L["k_pool"][l], L["v_pool"][l], kns[l], vns[l], L["slots"], positions,
+                                    stream=stream)
+            elif L["slots"] is not None:
+                pg.kv_append(L["k_pool"][l], L["v_pool"][l], kns[l], vns[l], L["slots"], stream=stream)
+            pg.run(plan.handle, qs[l], L["k_pool"][l], L["v_pool"][l], out=outs[l],
+                   pool_stable=L["slots"] is None, stream=stream)
 
-    # inputs: layer 0 alone, then doubling chunks that stay ahead of the layers; outputs:
-    # large chunks early and a one-layer chunk last, so little is left after the last layer
-    in_chunks = chunks(layers, [1, 1])
-    out_chunks = [(layers - b, layers - a) for a, b in reversed(chunks(layers, [1, 1]))]
-
-    def e2e_calls():
+    def e2e_calls(b):
         fork = torch.cuda.Event()
         fork.record(stream)
         h2d.wait_event(fork)
         d2h.wait_event(fork)
-        ev_in = {}
         with torch.cuda.stream(h2d):
-            for a, b in in_chunks:
-                sl = slice(a * per_layer_in, b * per_layer_in)
-                L["inputs"][sl].copy_(host_in[sl], non_blocking=True)
-                ev_in[a] = torch.cuda.Event()
-                ev_in[a].record(h2d)
-        ev_done = {}
-        for l in range(layers):
-            if l in ev_in:
-                stream.wait_event(ev_in[l])
-            if fused:
-                pg.append_run(plan.handle, L["k_new"][l], L["v_new"][l], L["q"][l], L["k_pool"][l],
-                              L["v_pool"][l], out=L["out"][l], pool_stable=True, stream=stream)
-            else:
-                if L["slots"] is not None and positions is not None:
-                    plan.kv_append_rope(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l],
-                                        L["slots"], positions, stream=stream)
-                elif L["slots"] is not None:
-                    pg.kv_append(L["k_pool"][l], L["v_pool"][l], L["k_new"][l], L["v_new"][l], L["slots"],
-                                 stream=stream)
-                pg.run(plan.handle, L["q"][l], L["k_pool"][l], L["v_pool"][l], out=L["out"][l],
-                       pool_stable=L["slots"] is None, stream=stream)
-            if any(b == l + 1 for _, b in out_chunks):
-                ev_done[l + 1] = torch.cuda.Event()
-                ev_done[l + 1].record(stream)
+            bufsets[1 - b][0].copy_(host_in, non_blocking=True)   # the next step's inputs
         with torch.cuda.stream(d2h):
-            for a, b in out_chunks:
-                d2h.wait_event(ev_done[b])
-                host_out[a:b].copy_(L["out"][a:b], non_blocking=True)
-        join = torch.cuda.Event()
-        join.record(d2h)
-        stream.wait_event(join)
+            host_out.copy_(bufsets[1 - b][4], non_blocking=True)  # the previous step's outputs
+        layers_on(bufsets[b])
+        for s in (h2d, d2h):
+            join = torch.cuda.Event()
+            join.record(s)
+            stream.wait_event(join)
 
     if graphs:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            e2e_calls()
-        graphs["e2e"] = g
+        for b in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                e2e_calls(b)
+            graphs[f"e2e{b}"] = g
         torch.cuda.synchronize()
 
-    def e2e_step():
+    def e2e_run(steps):
         if graphs:
-            update_plan()
-            graphs["e2e"].replay()
+            L["inputs"].copy_(host_in, non_blocking=True)  # the first step's inputs
+            for s in range(steps):
+                update_plan()
+                graphs[f"e2e{s % 2}"].replay()
+            host_out.copy_(bufsets[(steps - 1) % 2][4], non_blocking=True)  # the last step's outputs
             return
-        L["inputs"].copy_(host_in, non_blocking=True)
-        step()
-        host_out.copy_(L["out"], non_blocking=True)
+        for _ in range(steps):
+            L["inputs"].copy_(host_in, non_blocking=True)
+            step()
+            host_out.copy_(L["out"], non_blocking=True)
 
     def timed(fn, steps):
         barrier(world)
@@ -465,9 +449,9 @@ def run_ours(args, rank, world, local):
     run_reps = max(args.steps, 1)
     t_run = max_over_ranks(timed(lambda: replay("run_only", False), run_reps), world, device)
     with torch.cuda.stream(stream):
-        for _ in range(min(args.warmup, 10)):
-            e2e_step()
-    t_e2e = max_over_ranks(timed(e2e_step, args.steps), world, device)
+        e2e_run(max(2, min(args.warmup, 10)))
+    e2e_steps = max(args.steps, 2)
+    t_e2e = max_over_ranks(timed(lambda: e2e_run(e2e_steps), 1), world, device)
     clocks = sampler.stop()
 
     # host time of one plan update (validation, work list, one staged H2D copy), GPU idle
@@ -503,9 +487,9 @@ def run_ours(args, rank, world, local):
     # the committed counters describe the default launch of this workload only
     default_launch = (args.decode_kernel != "cuda_core" and not args.rope_theta and not args.split_tokens and
                       args.prefill_kernel == "auto" and not args.prefill_splits and
-                      not args.max_splits and not args.stages and not args.decode_ctas and not args.ctas_per_sm)
+                      not args.max_splits and not args.stages and not args.ctas_per_sm)
     traffic = profiled_traffic(args.workload) if default_launch else None
-    e2e_value = sum_over_ranks(b["per_step"] * args.steps, world, device) / t_e2e / 1e9
+    e2e_value = sum_over_ranks(b["per_step"] * e2e_steps, world, device) / t_e2e / 1e9
     if info["num_items"] == 0 and info["num_prefill_tiles"] > 0:
         # only multi-row requests: the prefill-segment kernel (a contraction) dominates
         flops = W.algorithmic_flops(w)
@@ -710,8 +694,6 @@ def main(argv=None):
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto")
     ap.add_argument("--stages", type=int, default=0, choices=[0, 2, 3], help="pipeline stages per warp")
-    ap.add_argument("--decode-ctas", type=int, default=0,
-                    help="0: one CTA per work item; n: n persistent CTAs; -1: one persistent CTA per SM")
     ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
     ap.add_argument("--prefill-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto")
