@@ -34,9 +34,8 @@
 //   S ready (tcgen05.commit, one per S buffer) -> the softmax of tile k;
 //   P ready (256 arrivals, two barriers by tile parity): P of tile k (and any scaled
 //     row of O) is in TMEM -> P.V of tile k;
-//   P.V done (tcgen05.commit, two by parity) -> a rescale of O and the final read of O.
-//   (An S buffer is reused without a wait: its last reader, a P.V product, was issued
-//   earlier by the same thread, and one thread's products run in issue order.)
+//   P.V done (tcgen05.commit, two by parity) -> a rescale of O, the final read of O, and
+//     the reuse of the tile's S buffer.
 // With three S buffers (d = 64) S runs two tiles ahead of P.V, so the threads find
 // each tile's scores ready.  Every wait is bounded; a thread whose wait gives up
 // reports it, stops waiting and still takes part in every barrier, so the CTA ends.
@@ -319,12 +318,11 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
                 }
                 pv_issued = kt;
             }
-            // S of tile kt + NSB - 1 goes in the S buffer of tile kt - 1.  Its last reader, the
-            // P.V of tile kt - 1, was issued earlier by this thread, and the products one thread
-            // issues run in issue order, so no wait for it is needed (measured on GB300: the
-            // wait took ~320 cycles a tile; without it the 512-row chunk runs 17.2 us against
-            // 17.4, the ragged call 34.2 against 35.3).
-            if (kt + C::NSB - 1 < ntiles && live) stage_s(kt + C::NSB - 1);
+            // S of tile kt + NSB - 1 goes in the S buffer of tile kt - 1, whose P.V (its last
+            // reader) must be done
+            if (kt + C::NSB - 1 < ntiles && live &&
+                (kt == 0 || wait_all(bar_o + 8 * ((kt - 1) & 1), ((kt - 1) >> 1) & 1)))
+                stage_s(kt + C::NSB - 1);
         }
         // drain what is still in flight (bounded; immediate when every wait succeeded): the
         // last commit on each barrier, which is the only phase a wait can still name
