@@ -98,3 +98,21 @@ def test_fused_rejects_cuda_core_plan_and_short_requests():
     with pytest.raises(pg.PagedGQAError) as e:
         p2.append_run(kn, kn, d2["q"], d2["k_pool"], d2["v_pool"])
     assert e.value.name == "PGQA_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_wide_form_boundaries(head_dim):
+    """Rows around the decode kernel's wide form (ten warps of one tile: up to 320 keys at
+    d 64, 160 at d 128), whose appended row lands in every warp's tile in turn: the fused
+    step and append-then-run against the oracle, under the plan's choice, the wide form
+    forced and forced splits."""
+    tile = 32 if head_dim == 64 else 16
+    lens = sorted({n for k in range(1, 11) for n in (k * tile - 1, k * tile, k * tile + 1)})
+    w = W.custom("wideb", lens, 16, 14, 2, head_dim, "bf16", 512, seed=head_dim + 11, append_last=True)
+    ro, rl = H.oracle_outputs(w)
+    for opts in ({}, {"pipeline_stages": 1}, {"split_tokens": 2 * tile}):
+        out, lse, dev, _ = fused_gpu(w, **opts)
+        H.compare(out, lse, ro, rl, f"fused wide boundaries d{head_dim} {opts}")
+        check_pool(w, dev)
+        out, lse, _ = H.gpu_outputs(w, **opts)
+        H.compare(out, lse, ro, rl, f"wide boundaries d{head_dim} {opts}")

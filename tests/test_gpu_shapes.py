@@ -241,3 +241,4 @@ def test_zero_sized_calls():
     torch.cuda.synchronize()
     assert torch.equal(k_pool, before_k) and torch.equal(v_pool, before_v)
     assert pg.read_device_flags() == 0
+
