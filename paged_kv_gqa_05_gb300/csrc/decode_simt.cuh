@@ -84,11 +84,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     uint8_t *pbuf = smem + C::PIPE_BYTES + C::BAR_BYTES + warp * C::PB_WARP + gi * C::PB_GROUP;
     const uint32_t bar0 = smem_addr(smem + C::PIPE_BYTES) + warp * C::ST * 8;
 
-    // The work list is written by plan_update's copy, never by a kernel, so it
-    // may be read before the programmatic-dependency wait.
-    pdl_launch_dependents();  // the next grid waits for our completion before touching our outputs
     if (smem_addr(smem) & 127u) {  // the stage layout assumes this alignment of the window
         if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_SMEM_ALIGN);
+        pdl_wait();  // completion order: this grid ends after the one before it
         return;
     }
     // The work list and kv_indices are final once plan_update is enqueued, so they
@@ -111,6 +109,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 2)
     __syncthreads();
 
     pdl_wait();
+    // Our predecessors are complete from here on, so a grid launched early after this
+    // trigger never overlaps a kernel older than this one.
+    pdl_launch_dependents();
 
     // Lane 0: resolve the pages of warp tile k and issue its K and V boxes.
     auto issue = [&](int k) {
