@@ -135,8 +135,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 }
 
 // Short slice lists (<= 32 per row): one warp per (task, head).  Lane s holds the
-// weight of slice s; each lane owns D/32 consecutive channels of every slice.
-template <typename OutT, int D>
+// weight of slice s; each lane owns D/32 consecutive channels of every slice.  The
+// partials of the first P slices are requested up front; P follows the call's longest
+// list (4, 8 or 16), since registers held for slices a call does not have cost
+// occupancy beside the decode grid (timed on GB300: 32 mixed-length rows of 10 slices,
+// 13.27 against 13.61 us per layer with P = 16 instead of 8; the ragged call, rows of
+// 2-3 slices, 38.0 us with P = 4, 38.2 with 8, 38.5 with 16).
+template <typename OutT, int D, int P>
 __global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, int units) {
     pdl_launch_dependents();
     constexpr int V = D / 32;  // channels per lane: 2 (D = 64) or 4 (D = 128)
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, in
     // (they do not depend on the weights): one memory latency before the fold, not two.
     const float *base = p.partial_o + (static_cast<size_t>(t.slot_base) * G + h) * D + lane * V;
     const size_t stride = static_cast<size_t>(G) * D;
-    constexpr int kPrefetch = 8;
+    constexpr int kPrefetch = P;
     float pre[kPrefetch][V];
 #pragma unroll
     for (int s = 0; s < kPrefetch; ++s) {
@@ -227,8 +232,14 @@ cudaError_t launch_merge_t(const MergeParams &p, int num_tasks, int max_splits, 
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 64>, p, units)
-                                : cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 128>, p, units);
+        if (max_splits <= 4)
+            return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 64, 4>, p, units)
+                                    : cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 128, 4>, p, units);
+        if (max_splits <= 8)
+            return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 64, 8>, p, units)
+                                    : cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 128, 8>, p, units);
+        return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 64, 16>, p, units)
+                                : cudaLaunchKernelEx(&cfg, merge_warp_kernel<OutT, 128, 16>, p, units);
     }
     const size_t smem = (32 * kChunk + 8 + static_cast<size_t>(max_splits)) * sizeof(float);
     auto kern = merge_kernel<OutT>;
