@@ -294,9 +294,7 @@ def run_ours(args, rank, world, local):
                    ctas_per_sm=args.ctas_per_sm, decode_kernel=args.decode_kernel,
                    pipeline_stages=args.stages,
                    rope_theta=args.rope_theta, rope_max_position=int(w.kv_lens.max()) if args.rope_theta > 0 else 0,
-                   prefill_kernel=args.prefill_kernel, prefill_splits=args.prefill_splits,
-                   split_combine=args.split_combine if args.split_combine in ("auto", "merge_kernel")
-                   else int(args.split_combine))
+                   prefill_kernel=args.prefill_kernel, prefill_splits=args.prefill_splits)
     stream = torch.cuda.Stream(device)
     positions = (torch.from_numpy(W.row_positions(w)).to(device)
                  if args.rope_theta > 0 and L["slots"] is not None else None)
@@ -489,8 +487,7 @@ def run_ours(args, rank, world, local):
     # the committed counters describe the default launch of this workload only
     default_launch = (args.decode_kernel != "cuda_core" and not args.rope_theta and not args.split_tokens and
                       args.prefill_kernel == "auto" and not args.prefill_splits and
-                      not args.max_splits and not args.stages and not args.ctas_per_sm and
-                      args.split_combine == "auto")
+                      not args.max_splits and not args.stages and not args.ctas_per_sm)
     traffic = profiled_traffic(args.workload) if default_launch else None
     e2e_value = sum_over_ranks(b["per_step"] * e2e_steps, world, device) / t_e2e / 1e9
     if info["num_items"] == 0 and info["num_prefill_tiles"] > 0:
@@ -538,7 +535,7 @@ def run_ours(args, rank, world, local):
             "rope_theta": args.rope_theta if args.rope_theta > 0 else None,
             "prefill_kernel": args.prefill_kernel if w.qo_indptr is not None else None,
             "plan": {k: info[k] for k in ("num_items", "num_merge_tasks", "split_tokens", "max_splits_used",
-                                          "num_sms", "cluster")},
+                                          "num_sms")},
         },
         "us_per_layer": round(t_dev / args.steps / layers * 1e6, 3),
         "us_per_run_call": round(t_run / (run_reps * layers) * 1e6, 3),
@@ -701,8 +698,6 @@ def main(argv=None):
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
     ap.add_argument("--prefill-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto")
     ap.add_argument("--prefill-splits", type=int, default=0, help="key slices per prefill tile (0: automatic)")
-    ap.add_argument("--split-combine", default="auto",
-                    help="split decode rows: auto | merge_kernel | a cluster size 2, 4, 8 or 16")
     ap.add_argument("--rope-theta", type=float, default=0.0,
                     help="> 0: rotary embedding of q and the appended K rows with this base")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define PGQA_ABI_VERSION 6
+#define PGQA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define PGQA_API __attribute__((visibility("default")))
@@ -149,20 +149,7 @@ typedef struct pgqa_plan_config {
                              PGQA_FLAG_WAIT_TIMEOUT and ends with the CTA (whose output
                              is then meaningless), instead of hanging.  Only that
                              kernel's per-item schedule honours it. */
-    int split_combine;    /* how the slices of a split decode row are combined:
-                             PGQA_COMBINE_AUTO, PGQA_COMBINE_MERGE_KERNEL (partials in global
-                             memory, merged by a second grid), or a cluster size 2, 4, 8 or
-                             16: the decode grid runs in thread-block clusters of that many
-                             CTAs, every split row's slices share one cluster (slices are
-                             lengthened until a row has at most that many), and the row's
-                             last slice folds the others in through distributed shared
-                             memory, with no second grid.  Clusters need the tensor-core
-                             kernel and groups of at most 8 heads; a call with prefill
-                             rows uses the merge kernel for all of its rows. */
 } pgqa_plan_config;
-
-#define PGQA_COMBINE_AUTO 0
-#define PGQA_COMBINE_MERGE_KERNEL 1
 
 #define PGQA_PREFILL_AUTO 0
 #define PGQA_PREFILL_TCGEN05 1
@@ -383,8 +370,6 @@ typedef struct pgqa_plan_info {
     int num_sms;            /* SMs of the plan's device */
     int64_t kv_tokens;      /* sum of kv_len over requests */
     int num_prefill_tiles;  /* CTAs of the prefill-segment kernel (requests with > 1 query row) */
-    int cluster;            /* > 1: the decode CTAs run in clusters of this size and combine split
-                               rows there (num_items then counts padding CTAs); 0: merge kernel */
 } pgqa_plan_info;
 
 PGQA_API pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info);
@@ -461,8 +446,6 @@ typedef struct pgqa_schedule_info {
     int pipeline_stages;    /* the tensor-core decode kernel's depth, 2 or 3; 1 = its wide form */
     int total_q_rows;
     int64_t kv_tokens;      /* sum of kv_len over requests */
-    int cluster;            /* as in pgqa_plan_info: slice i runs in cluster i / cluster; padding
-                               slices have q_row -1 */
 } pgqa_schedule_info;
 
 PGQA_API pgqa_status pgqa_plan_schedule(const pgqa_plan_config *cfg, int num_sms, const int32_t *kv_indptr_host,

@@ -49,21 +49,21 @@ class PlanConfig(ctypes.Structure):
                 ("pipeline_stages", ctypes.c_int), ("prefill_splits", ctypes.c_int),
                 ("rope_max_position", ctypes.c_int),
                 ("rope_theta", ctypes.c_double), ("prefill_kernel", ctypes.c_int),
-                ("test_stall_wait_us", ctypes.c_int), ("split_combine", ctypes.c_int)]
+                ("test_stall_wait_us", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("num_items", ctypes.c_int), ("num_merge_tasks", ctypes.c_int),
                 ("split_tokens", ctypes.c_int), ("max_splits_used", ctypes.c_int),
                 ("total_q_rows", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("kv_tokens", ctypes.c_int64), ("num_prefill_tiles", ctypes.c_int), ("cluster", ctypes.c_int)]
+                ("kv_tokens", ctypes.c_int64), ("num_prefill_tiles", ctypes.c_int)]
 
 
 class ScheduleInfo(ctypes.Structure):
     _fields_ = [("num_items", ctypes.c_int), ("num_merge_tasks", ctypes.c_int),
                 ("num_prefill_tiles", ctypes.c_int), ("split_tokens", ctypes.c_int),
                 ("max_splits_used", ctypes.c_int), ("pipeline_stages", ctypes.c_int),
-                ("total_q_rows", ctypes.c_int), ("kv_tokens", ctypes.c_int64), ("cluster", ctypes.c_int)]
+                ("total_q_rows", ctypes.c_int), ("kv_tokens", ctypes.c_int64)]
 
 
 # Rows of pgqa_plan_schedule's output arrays (pgqa_slice, pgqa_merge, pgqa_prefill_tile): int32 fields.
@@ -123,7 +123,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pgqa_plan_schedule.argtypes = [ctypes.POINTER(PlanConfig), ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int,
                                        _i32p, ctypes.c_int64, ctypes.c_int, _vp, ctypes.c_int, _vp, ctypes.c_int,
                                        _vp, ctypes.c_int, ctypes.POINTER(ScheduleInfo)]
-    if lib.pgqa_abi_version() != 6:
+    if lib.pgqa_abi_version() != 5:
         raise RuntimeError("libpagedgqa.so ABI version mismatch")
     _lib = lib
     return lib
@@ -204,14 +204,13 @@ def kv_append_rope(plan: int, k_pool: torch.Tensor, v_pool: torch.Tensor, k: tor
 def _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits=0,
             split_tokens=0, ctas_per_sm=0, decode_kernel="auto", pipeline_stages=0, prefill_splits=0,
             rope_theta=0.0, rope_max_position=0, prefill_kernel="auto",
-            test_stall_wait_us=0, split_combine="auto") -> PlanConfig:
+            test_stall_wait_us=0) -> PlanConfig:
     kinds = {"auto": 0, "tensor_core": 1, "cuda_core": 2}
     pf_kinds = {"auto": 0, "tcgen05": 1, "mma_sync": 2}
-    combine = {"auto": 0, "merge_kernel": 1}.get(split_combine, split_combine)
     return PlanConfig(num_qo_heads, num_kv_heads, head_dim, page_size, TORCH_TO_CODE[dtype],
                       max_batch, max_q_rows, max_splits, split_tokens, ctas_per_sm, kinds[decode_kernel],
                       pipeline_stages, prefill_splits, rope_max_position, float(rope_theta),
-                      pf_kinds[prefill_kernel], int(test_stall_wait_us), int(combine))
+                      pf_kinds[prefill_kernel], int(test_stall_wait_us))
 
 
 def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
@@ -219,16 +218,15 @@ def plan_create(num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: 
                 split_tokens: int = 0, ctas_per_sm: int = 0, decode_kernel: str = "auto",
                 pipeline_stages: int = 0, prefill_splits: int = 0,
                 rope_theta: float = 0.0, rope_max_position: int = 0, prefill_kernel: str = "auto",
-                test_stall_wait_us: int = 0, split_combine="auto") -> int:
+                test_stall_wait_us: int = 0) -> int:
     """pgqa_plan_create on the current CUDA device; returns the plan handle.
     decode_kernel: "auto" | "tensor_core" | "cuda_core"; rope_theta > 0 turns on the
     rotary embedding of q and the appended K rows (positions < rope_max_position);
     prefill_kernel: "auto" | "tcgen05" | "mma_sync"; test_stall_wait_us > 0 only in
-    the test of the bounded-wait failure path (see pgqa_plan_config); split_combine:
-    "auto" | "merge_kernel" | a cluster size 2, 4, 8 or 16."""
+    the test of the bounded-wait failure path (see pgqa_plan_config)."""
     cfg = _config(num_qo_heads, num_kv_heads, head_dim, page_size, dtype, max_batch, max_q_rows, max_splits,
                   split_tokens, ctas_per_sm, decode_kernel, pipeline_stages, prefill_splits,
-                  rope_theta, rope_max_position, prefill_kernel, test_stall_wait_us, split_combine)
+                  rope_theta, rope_max_position, prefill_kernel, test_stall_wait_us)
     h = _vp()
     _check(load().pgqa_plan_create(ctypes.byref(h), ctypes.byref(cfg)))
     return h.value

@@ -3,7 +3,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <cstddef>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -177,7 +176,6 @@ struct pgqa_plan {
     int prefill_kind = PGQA_PREFILL_TCGEN05;  // prefill-segment kernel
     int prefill_pairs = 128;                  // (row, head) pairs per prefill tile of that kernel
     int stages = 2;     // per-warp pipeline depth of the tensor-core kernel (chosen per plan_update)
-    int cluster = 0;    // > 1: decode CTAs run in clusters of this size, split rows combined there
     int max_items = 0;  // capacity of the work list and of the partial slots
     int max_tasks = 0;
     int max_prefill = 0;     // capacity of the prefill-tile list
@@ -250,14 +248,6 @@ static void plan_free(pgqa_plan *p) {
     if (p->rope_cs) cudaFree(p->rope_cs);
     delete p;
 }
-
-// The layouts the ctypes binding mirrors (natural C alignment).
-static_assert(offsetof(pgqa_plan_config, test_stall_wait_us) == 76 && offsetof(pgqa_plan_config, split_combine) == 80 &&
-                  sizeof(pgqa_plan_config) == 88,
-              "pgqa_plan_config layout");
-static_assert(offsetof(pgqa_plan_info, cluster) == 36 && sizeof(pgqa_plan_info) == 40, "pgqa_plan_info layout");
-static_assert(offsetof(pgqa_schedule_info, cluster) == 40 && sizeof(pgqa_schedule_info) == 48,
-              "pgqa_schedule_info layout");
 
 // Helpers shared with the other entry-point translation units.
 namespace pgqa {
@@ -385,13 +375,6 @@ static pgqa_status check_config(const pgqa_plan_config &c) {
     if (c.pipeline_stages == 1 && (c.decode_kernel == PGQA_DECODE_CUDA_CORE || group > 8))
         return fail(PGQA_ERR_UNSUPPORTED, "the wide decode form (pipeline_stages 1) runs groups of up to 8 heads "
                     "on the per-item tensor-core kernel");
-    const int sc = c.split_combine;
-    if (sc != PGQA_COMBINE_AUTO && sc != PGQA_COMBINE_MERGE_KERNEL && sc != 2 && sc != 4 && sc != 8 && sc != 16)
-        return fail(PGQA_ERR_INVALID_ARG, "split_combine %d (0, 1, or a cluster size 2, 4, 8 or 16)", sc);
-    if (sc > 1 && (c.decode_kernel == PGQA_DECODE_CUDA_CORE || group > 8))
-        return fail(PGQA_ERR_UNSUPPORTED, "the cluster combine runs groups of up to 8 heads on the tensor-core kernel");
-    if (sc > 1 && c.pipeline_stages == 1 && c.head_dim == 128)
-        return fail(PGQA_ERR_UNSUPPORTED, "the wide decode form at head_dim 128 has no room for the cluster combine");
     if (c.rope_theta < 0.0 || std::isnan(c.rope_theta)) return fail(PGQA_ERR_INVALID_ARG, "rope_theta %g", c.rope_theta);
     if (c.rope_theta > 0.0) {
         if (c.rope_max_position < 1 || c.rope_max_position > (1 << 24))
@@ -511,7 +494,6 @@ pgqa_status pgqa_plan_get_info(const pgqa_plan *plan, pgqa_plan_info *info) {
     info->num_sms = plan->num_sms;
     info->kv_tokens = plan->kv_tokens;
     info->num_prefill_tiles = plan->n_prefill;
-    info->cluster = plan->cluster;
     return PGQA_OK;
 }
 
@@ -664,79 +646,8 @@ struct Schedule {
     std::vector<PrefillItem> prefill;
     int64_t split_tokens = 0, rows = 0, kv_tokens = 0;
     int max_used = 1, max_task_splits = 0, stages = 2;
-    int cluster = 0;
     bool fusable = true;
 };
-
-// Cluster combine: lays the work items out in clusters of `cl` consecutive CTAs, the
-// slices of each split row (groups[i] = first item, count) contiguous inside one
-// cluster in slice order, so that the last slice (the leader) sits at the highest rank
-// of the row.  Rows of many slices are placed first, each into the first cluster with
-// room; single-slice items then fill the holes, longest first, and open new clusters;
-// what stays empty is padding (q_row -1).  Clusters holding the longest slices come
-// first, so that they start in the first wave.
-static std::vector<WorkItem> pack_clusters(const std::vector<WorkItem> &items,
-                                           const std::vector<std::pair<size_t, int>> &groups, int cl) {
-    auto len = [&](size_t i) { return items[i].tok_end - items[i].tok_begin; };
-    std::vector<char> grouped(items.size(), 0);
-    std::vector<std::pair<size_t, int>> multi(groups);
-    for (const auto &g : multi)
-        for (int k = 0; k < g.second; ++k) grouped[g.first + k] = 1;
-    std::stable_sort(multi.begin(), multi.end(), [&](const std::pair<size_t, int> &a, const std::pair<size_t, int> &b) {
-        return a.second != b.second ? a.second > b.second : len(a.first) > len(b.first);
-    });
-    std::vector<size_t> singles;
-    for (size_t i = 0; i < items.size(); ++i)
-        if (!grouped[i]) singles.push_back(i);
-    std::stable_sort(singles.begin(), singles.end(), [&](size_t a, size_t b) { return len(a) > len(b); });
-
-    struct Bin {
-        std::vector<size_t> idx;      // item indices in rank order
-        std::vector<int> first, cnt;  // per rank: the row's first rank and slice count (-1: single)
-    };
-    std::vector<Bin> bins;
-    for (const auto &g : multi) {
-        size_t b = 0;
-        while (b < bins.size() && static_cast<int>(bins[b].idx.size()) + g.second > cl) ++b;
-        if (b == bins.size()) bins.emplace_back();
-        Bin &bin = bins[b];
-        const int r0 = static_cast<int>(bin.idx.size());
-        for (int k = 0; k < g.second; ++k) {
-            bin.idx.push_back(g.first + k);
-            bin.first.push_back(r0);
-            bin.cnt.push_back(g.second);
-        }
-    }
-    size_t fill = 0;
-    for (size_t i : singles) {
-        while (fill < bins.size() && static_cast<int>(bins[fill].idx.size()) >= cl) ++fill;
-        if (fill == bins.size()) bins.emplace_back();
-        bins[fill].idx.push_back(i);
-        bins[fill].first.push_back(-1);
-        bins[fill].cnt.push_back(0);
-    }
-    std::vector<int32_t> longest(bins.size(), 0);
-    for (size_t b = 0; b < bins.size(); ++b)
-        for (size_t i : bins[b].idx) longest[b] = std::max(longest[b], len(i));
-    std::vector<size_t> order(bins.size());
-    for (size_t b = 0; b < order.size(); ++b) order[b] = b;
-    std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) { return longest[a] > longest[b]; });
-
-    std::vector<WorkItem> out;
-    out.reserve(bins.size() * cl);
-    const WorkItem pad = {0, 0, 0, -1, 0, -1, INT32_MAX, 0, -1, 0, -1, 0};
-    for (size_t b : order) {
-        const Bin &bin = bins[b];
-        for (size_t r = 0; r < bin.idx.size(); ++r) {
-            WorkItem w = items[bin.idx[r]];
-            w.cl_first = bin.first[r];
-            w.cl_count = bin.cnt[r];
-            out.push_back(w);
-        }
-        for (size_t r = bin.idx.size(); r < static_cast<size_t>(cl); ++r) out.push_back(pad);
-    }
-    return out;
-}
 
 static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indptr, const int32_t *last_page_len,
                                   const int32_t *qo_indptr, int batch, bool have_indices,
@@ -830,18 +741,12 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
     const int tile = plan->tile;
     int64_t longest = 0;
     for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
-    int64_t ls = c.split_tokens > 0 ? round_up(c.split_tokens, tile)
-                                    : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest,
-                                                   !prefill.empty());
-
-    // The cluster combine serves calls without prefill rows: every split row's slices in
-    // one cluster, so no row may have more slices than a cluster has CTAs.
-    const int cl = (c.split_combine > 1 && prefill.empty()) ? c.split_combine : 0;
-    if (cl > 1 && longest > 0) ls = std::max<int64_t>(ls, round_up(ceil_div(longest, cl), tile));
+    const int64_t ls = c.split_tokens > 0 ? round_up(c.split_tokens, tile)
+                                          : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest,
+                                                         !prefill.empty());
 
     std::vector<WorkItem> items;
     std::vector<MergeTask> tasks;
-    std::vector<std::pair<size_t, int>> groups;  // cluster combine: (first item, slices) of split rows
     items.reserve(static_cast<size_t>(rows) * c.num_kv_heads);
     int slot = 0, max_used = 1, max_task_splits = 0;
     for (const Row &rw : rowv) {
@@ -853,17 +758,7 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
             ns = n == 0 ? 1 : ceil_div(n, len);
             if (ns == 1) {
                 items.push_back({rw.page_base, 0, static_cast<int32_t>(n), rw.q_row, kvh, -1, rw.new_begin,
-                                 rw.new_row_base, rw.own_pos, rw.own_pos, -1, 0});
-                continue;
-            }
-            if (cl > 1) {  // the row's last slice folds in the others inside their cluster
-                groups.emplace_back(items.size(), static_cast<int>(ns));
-                for (int64_t s = 0; s < ns; ++s)
-                    items.push_back({rw.page_base, static_cast<int32_t>(s * len),
-                                     static_cast<int32_t>(std::min<int64_t>(n, (s + 1) * len)), rw.q_row, kvh, -1,
-                                     rw.new_begin, rw.new_row_base, s == ns - 1 ? rw.own_pos : -1, rw.own_pos, -1,
-                                     0});
-                max_used = std::max<int>(max_used, static_cast<int>(ns));
+                                 rw.new_row_base, rw.own_pos, rw.own_pos, 0, 0});
                 continue;
             }
             if (static_cast<int64_t>(tasks.size()) >= plan->max_tasks || slot + ns > plan->max_slots)
@@ -872,7 +767,7 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
                 items.push_back({rw.page_base, static_cast<int32_t>(s * len),
                                  static_cast<int32_t>(std::min<int64_t>(n, (s + 1) * len)), rw.q_row, kvh,
                                  slot + static_cast<int32_t>(s), rw.new_begin, rw.new_row_base,
-                                 s == ns - 1 ? rw.own_pos : -1, rw.own_pos, -1, 0});
+                                 s == ns - 1 ? rw.own_pos : -1, rw.own_pos, 0, 0});
             tasks.push_back({rw.q_row, kvh, slot, static_cast<int32_t>(ns)});
             slot += static_cast<int>(ns);
             max_used = std::max<int>(max_used, static_cast<int>(ns));
@@ -881,17 +776,10 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
         if (static_cast<int64_t>(items.size()) > plan->max_items)
             return fail(PGQA_ERR_CAPACITY, "work items exceed the plan capacity %d", plan->max_items);
     }
-    if (cl > 1) {
-        items = pack_clusters(items, groups, cl);
-        if (static_cast<int64_t>(items.size()) > plan->max_items)
-            return fail(PGQA_ERR_CAPACITY, "work items with cluster padding exceed the plan capacity %d",
-                        plan->max_items);
-    } else {
-        // Longest slices first, so that they start in the first wave.
-        std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &b) {
-            return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
-        });
-    }
+    // Longest slices first, so that they start in the first wave.
+    std::stable_sort(items.begin(), items.end(), [](const WorkItem &a, const WorkItem &b) {
+        return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
+    });
 
     // Prefill key slices (each >= 256 keys, at most 8), partials merged per (row, kv head)
     // like split decode rows.  Alone, a chunk takes the most slices that still fit one wave
@@ -956,7 +844,6 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
         int64_t longest_item = 0;
         for (const WorkItem &w : items) longest_item = std::max<int64_t>(longest_item, w.tok_end - w.tok_begin);
         stages = pick_stages(plan, longest_item, static_cast<int64_t>(items.size()), !prefill.empty());
-        if (cl > 1 && stages == 1 && c.head_dim == 128) stages = 2;  // the wide form has no room for it there
     }
     out->items.swap(items);
     out->tasks.swap(tasks);
@@ -967,7 +854,6 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
     out->max_used = max_used;
     out->max_task_splits = max_task_splits;
     out->stages = stages;
-    out->cluster = cl;
     out->fusable = fusable;
     return PGQA_OK;
 }
@@ -1016,7 +902,6 @@ pgqa_status pgqa_plan_update(pgqa_plan *plan, const int32_t *kv_indptr, const in
     plan->cur ^= 1;
 
     plan->stages = sc.stages;
-    plan->cluster = sc.cluster;
     plan->n_items = static_cast<int>(items.size());
     plan->n_prefill = static_cast<int>(prefill.size());
     plan->causal = causal != 0;
@@ -1067,7 +952,6 @@ pgqa_status pgqa_plan_schedule(const pgqa_plan_config *cfg, int num_sms, const i
     info->pipeline_stages = sc.stages;
     info->total_q_rows = static_cast<int>(sc.rows);
     info->kv_tokens = sc.kv_tokens;
-    info->cluster = sc.cluster;
     if ((slices && max_slices < info->num_items) || (merges && max_merges < info->num_merge_tasks) ||
         (tiles && max_tiles < info->num_prefill_tiles))
         return fail(PGQA_ERR_CAPACITY, "output arrays hold %d / %d / %d entries, the schedule has %d / %d / %d",
@@ -1190,7 +1074,6 @@ static pgqa_status run_impl(pgqa_plan *plan, const void *k_new, const void *v_ne
     p.defer_wait = plan->n_prefill > 0 ? 1 : 0;
     p.rope_cs = plan->rope_cs;
     p.stall_wait_us = static_cast<uint32_t>(c.test_stall_wait_us);
-    p.cluster = plan->cluster;
     e = launch_decode(plan->kernel, plan->stages, c.head_dim, plan->group, c.dtype, *mk, *mv, p, plan->n_items,
                       true, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");

@@ -29,10 +29,7 @@ struct alignas(16) WorkItem {
     int32_t new_row_base;  // the new row of key position p is k_new[p + new_row_base]
     int32_t write_pos;     // key position whose new row this item stores into the pool, or -1
     int32_t q_pos;         // key position of the query row's own key: its rotary position
-    int32_t cl_first;      // cluster combine: cluster rank of the first slice of this row's slices
-                           // (they hold ranks cl_first .. cl_first + cl_count - 1; the last is the
-                           // leader, which writes the row); -1 otherwise
-    int32_t cl_count;      // cluster combine: number of slices of the row (>= 2)
+    int32_t pad1, pad2;
 };
 static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
 
@@ -104,10 +101,6 @@ struct DecodeParams {
     uint32_t stall_wait_us;    // test hook of the per-item tensor-core kernel (0 = off): warp 0
                                // of every CTA withholds its first tile's copies and gives up
                                // waiting for them after this many microseconds
-    int cluster;               // > 1: launched in clusters of this many CTAs, and the slices of a
-                               // row (items with cl_first >= 0) combine inside their cluster
-                               // through distributed shared memory; items with q_row < 0 are
-                               // padding
 };
 
 struct PrefillParams {
@@ -148,7 +141,6 @@ struct MergeParams {
 };
 
 // Launchers (defined in the kernel translation units).  Decode: one CTA per work item.
-// Decode: one CTA per work item, in clusters of p.cluster CTAs when p.cluster > 1.
 cudaError_t launch_decode(int kind, int stages, int head_dim, int group, pgqa_dtype dtype, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, int num_items, bool pdl,
                           cudaStream_t stream);
@@ -304,62 +296,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Thread-block clusters (distributed shared memory).
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Every thread of the cluster arrives once after initialising its barriers; a thread
-// that later touches another CTA's shared memory (or barriers) waits first.  A thread
-// may exit without waiting.
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
-// The shared::cluster address of this CTA's shared-memory address `local` in CTA `rank`.
-__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float4 dsmem_ld128(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ float dsmem_ld32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-// One arrival on a barrier in another CTA of the cluster, ordering this thread's earlier
-// memory operations (and, through a preceding CTA barrier, its CTA's) before it.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// A bounded wait (~2 s) on this CTA's barrier whose arrivals come from other CTAs of the
-// cluster: acquire at cluster scope, so their memory operations before the arrival are
-// visible afterwards.  Returns false on giving up.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity), "r"(10000u)
-            : "memory");
-        if (ok) return true;
-        if ((it & 15u) == 15u && global_timer_ns() - t0 > 2000000000ull) return false;
-    }
-}
-
 // Hardware approximations (PTX ex2/lg2/rcp .approx): a few ulp, ample for the
 // softmax weights and the log-sum-exp.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -439,8 +375,8 @@ __device__ __forceinline__ WorkItem load_work_item(const WorkItem *src) {
     it.new_row_base = w[7];
     it.write_pos = w[8];
     it.q_pos = w[9];
-    it.cl_first = w[10];
-    it.cl_count = w[11];
+    it.pad1 = w[10];
+    it.pad2 = w[11];
     return it;
 }
 

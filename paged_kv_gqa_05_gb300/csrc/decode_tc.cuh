@@ -99,20 +99,13 @@ struct TcCfg {
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K tile, then V tile
     static constexpr int PIPE_BYTES = NW * ST * STAGE_BYTES;
-    static constexpr int BAR_BYTES = NW * ST * 8 + 16;   // per-warp stage barriers, then the cluster
-                                                         // combine's gather and release barriers
+    static constexpr int BAR_BYTES = NW * ST * 8;
     static constexpr int DT = D / 16;                    // d m-tiles of the PV product
     static constexpr int KS = D / 16;                    // k-steps of the QK product
     static constexpr int OS = D + 4;                     // padded row stride (floats) of a warp's O
     static constexpr int ROPE_BYTES = D * 4;             // one rotary table row: D/2 (cos, sin)
     static constexpr int SMEM_BYTES = PIPE_BYTES + BAR_BYTES + kSlicePageCap * 4 + ROPE_BYTES;
-    // Cluster combine: a slice's result, [8 heads][D + 4] floats (D channels, then its
-    // log2-sum-exp), at the end of the stage area, past the last warp's combine state.
-    static constexpr int RES_STRIDE = D + 4;
-    static constexpr int RES_BYTES = 8 * RES_STRIDE * 4;
-    static constexpr bool CLUSTER_OK = ST * STAGE_BYTES >= (16 + 8 * OS) * 4 + RES_BYTES;
     static_assert(HALF_BYTES % 1024 == 0, "128B-swizzled blocks start on 1024-byte boundaries");
-    static_assert((PIPE_BYTES + BAR_BYTES) % 16 == 0, "the rotary row stays 16-byte aligned");
 };
 
 // Byte offset of 16-byte chunk `c` (0..D/8-1) of tile row `r` inside a stage's
@@ -157,13 +150,6 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
     // copy sits between any earlier writer and this kernel), so they are read
     // before the grid-dependency wait; q and the new rows only after it.
     const WorkItem it = load_work_item(p.items + blockIdx.x);
-    if (it.q_row < 0) {  // padding of the last cluster
-        pdl_wait();
-        return;
-    }
-    // Cluster combine (CLUSTER_OK variants only; the plan launches no other in clusters).
-    const bool clu = C::CLUSTER_OK && NH == 1 && p.cluster > 1;
-    const uint32_t cl_bar = smem_addr(smem + C::PIPE_BYTES + C::NW * C::ST * 8);  // gather; release at + 8
     // The query row's rotary table row goes to shared memory.  The table is fixed since
     // plan creation, so it is read before the dependency wait, in flight together with
     // the page-table staging; the CTA barrier below publishes it.
@@ -177,10 +163,6 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
 
     if (lane == 0) {
         for (int s = 0; s < C::ST; ++s) mbar_init(bar0 + 8 * s, 1);
-        if (clu && warp == 0) {
-            mbar_init(cl_bar, it.cl_count > 2 ? it.cl_count - 1 : 1);  // one arrival per other slice
-            mbar_init(cl_bar + 8, 1);                                   // the leader's release
-        }
         fence_barrier_init();
         if (warp == 0) {
             prefetch_tensormap(&tm_k);
@@ -191,9 +173,6 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
         stage_slice_pages(page_buf, p.kv_indices, it.page_base, it.tok_begin, it.tok_end, p.page_size);
     if (ROPE && threadIdx.x < D / 4) reinterpret_cast<float4 *>(rope_row)[threadIdx.x] = rope_part;
     __syncthreads();
-    // Every CTA of a cluster arrives once its barriers are initialised; only a thread that
-    // later reaches into another CTA waits for that.
-    if (clu) cluster_arrive_release();
     const uint64_t policy = l2_evict_first_policy();
 
     auto issue = [&](int k) {
@@ -584,23 +563,6 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
     }
     __syncthreads();
 
-    // Cluster combine roles: the slices of a row hold ranks cl_first .. cl_first + cl_count - 1
-    // of the cluster; the last (the shortest) is the leader and writes the row.  The others
-    // leave their results in their own shared memory, signal the leader and stay resident
-    // until it has read them.
-    const int my_rank = clu ? static_cast<int>(cluster_ctarank()) : 0;
-    bool cl_row = clu && it.cl_first >= 0;
-    if (cl_row && (it.cl_count < 2 || it.cl_first + it.cl_count > p.cluster || my_rank < it.cl_first ||
-                   my_rank >= it.cl_first + it.cl_count)) {
-        // a work list this kernel cannot trust: no access to another CTA's memory
-        if (threadIdx.x == 0) atomicOr(p.flags, PGQA_FLAG_PAGE_INDEX);
-        cl_row = false;
-    }
-    const int lead = it.cl_first + it.cl_count - 1;
-    const bool contributor = cl_row && my_rank != lead;
-    const bool leader = cl_row && !contributor;
-    float *res = reinterpret_cast<float *>(pipe + C::PIPE_BYTES - C::RES_BYTES);  // [8][RES_STRIDE]
-
     constexpr int CH8 = D / 8;
     for (int idx = threadIdx.x; idx < G * CH8; idx += C::NW * 32) {
         const int h = idx / CH8;
@@ -630,45 +592,8 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
             acc[0] += a.x * f; acc[1] += a.y * f; acc[2] += a.z * f; acc[3] += a.w * f;
             acc[4] += b.x * f; acc[5] += b.y * f; acc[6] += b.z * f; acc[7] += b.w * f;
         }
-        float lse2 = (L == 0.f) ? -INFINITY : Mx + lg2_approx(L);
+        const float lse2 = (L == 0.f) ? -INFINITY : Mx + lg2_approx(L);
         const int head = it.kv_head * G + h;
-        if (contributor) {  // this slice's (O, lse) for the leader
-            float *r = res + h * C::RES_STRIDE;
-            *reinterpret_cast<float4 *>(r + c8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            *reinterpret_cast<float4 *>(r + c8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-            if (c8 == 0) r[D] = lse2;
-            continue;
-        }
-        if (leader) {
-            // Fold in the row's other slices, read from their shared memory: the same
-            // log-sum-exp merge as the merge kernel, one slice at a time.
-            if (!mbar_wait_cluster(cl_bar, 0)) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-            float m = lse2, sw = (lse2 == -INFINITY) ? 0.f : 1.f;
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[jj] *= sw;
-            const uint32_t off = smem_addr(res + h * C::RES_STRIDE);
-#pragma unroll 4
-            for (int j = 0; j < it.cl_count - 1; ++j) {
-                const uint32_t rb = dsmem_addr(off, static_cast<uint32_t>(it.cl_first + j));
-                const float lj = dsmem_ld32(rb + D * 4);
-                const float4 a = dsmem_ld128(rb + c8 * 4);
-                const float4 b = dsmem_ld128(rb + c8 * 4 + 16);
-                if (lj == -INFINITY) continue;  // no admissible key in that slice
-                const float mn = fmaxf(m, lj);  // a NaN lse propagates through wj
-                const float f = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-                const float wj = ex2_approx(lj - mn);
-                sw = sw * f + wj;
-                acc[0] = acc[0] * f + wj * a.x; acc[1] = acc[1] * f + wj * a.y;
-                acc[2] = acc[2] * f + wj * a.z; acc[3] = acc[3] * f + wj * a.w;
-                acc[4] = acc[4] * f + wj * b.x; acc[5] = acc[5] * f + wj * b.y;
-                acc[6] = acc[6] * f + wj * b.z; acc[7] = acc[7] * f + wj * b.w;
-                m = mn;
-            }
-            const float inv_s = (sw == 0.f) ? 0.f : rcp_approx(sw);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[jj] *= inv_s;
-            lse2 = (sw == 0.f) ? -INFINITY : m + lg2_approx(sw);
-        }
         if (it.out_slot < 0) {
             const size_t oi = (static_cast<size_t>(it.q_row) * p.num_qo_heads + head) * D + c8;
             if (p.out_dtype == PGQA_FP32) {
@@ -693,25 +618,6 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
             if (c8 == 0) p.partial_lse[slot] = lse2;
         }
     }
-    if (contributor) {  // CTA-uniform
-        __syncthreads();  // the results are in shared memory
-        if (threadIdx.x == 0) {
-            cluster_wait_acquire();  // the leader's barriers are initialised
-            mbar_arrive_remote(dsmem_addr(cl_bar, static_cast<uint32_t>(lead)));
-            // stay resident (this thread holds the CTA) until the leader has read our results
-            if (!mbar_wait_cluster(cl_bar + 8, 0)) atomicOr(p.flags, PGQA_FLAG_WAIT_TIMEOUT);
-        }
-    } else if (leader) {
-        __syncthreads();  // every read of the other slices' results is done
-        if (threadIdx.x == 0) {
-            cluster_wait_acquire();  // their release barriers are initialised
-            for (int j = 0; j < it.cl_count - 1; ++j)
-                mbar_arrive_remote(dsmem_addr(cl_bar + 8, static_cast<uint32_t>(it.cl_first + j)));
-        }
-    }
-    // Every thread of a cluster launch completes its arrival's phase before leaving (all
-    // arrived right after their start, so this returns at once).
-    if (clu) cluster_wait_acquire();
 }
 
 // Raises the kernel's dynamic shared-memory limit once per device.
@@ -726,11 +632,6 @@ cudaError_t configure_decode_tc() {
         e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, ROPE, T, NW>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<D, STAGES, NW>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        if (TcCfg<D, STAGES, NW>::CLUSTER_OK && NH == 1) {  // clusters of 16 CTAs are beyond the portable 8
-            e = cudaFuncSetAttribute(decode_tc_kernel<D, STAGES, NH, ROPE, T, NW>,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     return cudaSuccess;
@@ -747,19 +648,11 @@ cudaError_t launch_decode_tc_st(int group, const CUtensorMap &tm_k, const CUtens
     cfg.blockDim = dim3(C::NW * 32);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.cluster > 1) {
-        if (!C::CLUSTER_OK || NH != 1 || num_items % p.cluster != 0) return cudaErrorInvalidValue;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-    }
     return cudaLaunchKernelEx(&cfg, decode_tc_kernel<D, STAGES, NH, ROPE, T, NW>, tm_k, tm_v, p, group);
 }
 

@@ -103,8 +103,7 @@ __global__ void build_static_work(const int32_t *__restrict__ kv_indptr, const i
     w.new_row_base = 0;
     w.write_pos = -1;
     w.q_pos = n > 0 ? n - 1 : 0;  // unused: this entry point has no rotary embedding
-    w.cl_first = -1;  // no cluster combine on this path
-    w.cl_count = 0;
+    w.pad1 = w.pad2 = 0;
     items[i] = w;
     if (s == 0 && splits > 1) tasks[t] = MergeTask{b, kvh, t * splits, splits};
 }

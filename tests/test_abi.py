@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.pgqa_abi_version() == 6
+    assert lib.pgqa_abi_version() == 5
     for code in range(7):
         assert lib.pgqa_status_string(code)
 
@@ -82,16 +82,7 @@ def test_plan_config_layout():
     PC = binding.PlanConfig
     assert PC.max_q_rows.offset == 24 and PC.prefill_splits.offset == 52
     assert PC.rope_max_position.offset == 56 and PC.rope_theta.offset == 64
-    assert PC.prefill_kernel.offset == 72 and PC.test_stall_wait_us.offset == 76
-    assert PC.split_combine.offset == 80 and ctypes.sizeof(PC) == 88
-    assert B_info_layout()
-
-
-def B_info_layout():
-    """The info structs end with the cluster size (after an int64 and an int)."""
-    from paged_kv_gqa_05_gb300 import binding
-    return (binding.PlanInfo.cluster.offset == 36 and ctypes.sizeof(binding.PlanInfo) == 40 and
-            binding.ScheduleInfo.cluster.offset == 40 and ctypes.sizeof(binding.ScheduleInfo) == 48)
+    assert PC.prefill_kernel.offset == 72 and PC.test_stall_wait_us.offset == 76 and ctypes.sizeof(PC) == 80
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -35,34 +35,20 @@ def check_schedule(w, sc, prefill_rows_on_tiles=True):
     assert info["total_q_rows"] == int(qo[-1]) and info["kv_tokens"] == int(kv_lens.sum())
     assert info["pipeline_stages"] in (1, 2, 3)
 
-    # launch order: longest slices first; with the cluster combine, clusters of C
-    # consecutive slices, the cluster holding the longest slice first, padded with q_row -1
-    C = info["cluster"]
+    # launch order: longest slices first
     lens = slices["key_end"] - slices["key_begin"]
     if info["pipeline_stages"] == 1 and len(lens):
         # the wide form: one warp tile per warp (ten warps) unless the caller forced it
         assert G <= 8
-    real = slices["q_row"] >= 0
-    if C > 1:
-        assert C in (2, 4, 8, 16) and len(slices) % C == 0 and not len(merges)
-        assert np.all(lens[~real] == 0) and np.all(slices["partial_slot"] == -1)
-        assert np.all(slices["append_pos"][~real] == -1)
-        assert np.all(np.diff(lens.reshape(-1, C).max(axis=1)) <= 0), "clusters are not longest-first"
-        assert not (w.head_dim == 128 and info["pipeline_stages"] == 1), "the d128 wide form has no cluster combine"
-    else:
-        assert C == 0 and np.all(real)
-        assert np.all(np.diff(lens) <= 0), "slices are not longest-first"
+    assert np.all(np.diff(lens) <= 0), "slices are not longest-first"
     assert np.all(slices["key_begin"] % tile == 0)
 
     merge_of = {(int(m["q_row"]), int(m["kv_head"])): m for m in merges}
     assert len(merge_of) == len(merges), "two merges for one (row, kv head)"
     used_slots = set()
     by_pair = defaultdict(list)
-    positions = defaultdict(list)  # launch positions of each pair's slices
-    for i, s in enumerate(slices):
-        if s["q_row"] >= 0:
-            by_pair[(int(s["q_row"]), int(s["kv_head"]))].append(s)
-            positions[(int(s["q_row"]), int(s["kv_head"]))].append(i)
+    for s in slices:
+        by_pair[(int(s["q_row"]), int(s["kv_head"]))].append(s)
 
     expected_pairs = set()
     merged_pairs = set()
@@ -90,11 +76,6 @@ def check_schedule(w, sc, prefill_rows_on_tiles=True):
                     assert not writers
                 if len(ss) == 1:
                     assert ss[0]["partial_slot"] == -1 and (r, kvh) not in merge_of
-                elif C > 1:  # consecutive ranks of one cluster, in key order
-                    idx = positions[(r, kvh)]
-                    assert len(ss) <= C and idx == list(range(idx[0], idx[0] + len(ss))), idx
-                    assert idx[0] // C == idx[-1] // C, f"row {r} kv head {kvh} spans two clusters"
-                    assert [int(x["key_begin"]) for x in by_pair[(r, kvh)]] == [b for b, _ in bounds]
                 else:
                     m = merge_of[(r, kvh)]
                     merged_pairs.add((r, kvh))
@@ -341,53 +322,3 @@ def test_prefill_slices_leave_room_for_decode_rows():
     mixed = schedule(W.make("ragged"))["info"]
     assert SMS < alone["num_prefill_tiles"] <= 2 * SMS
     assert mixed["num_items"] > 0 and mixed["num_prefill_tiles"] <= SMS
-
-
-@pytest.mark.parametrize("cl", [2, 4, 8, 16])
-@pytest.mark.parametrize("name", ["tiny", "qwen05_decode", "qwen15_mixed", "long_context_b1", "long_context_b4",
-                                  "wide_group_d64"])
-def test_cluster_combine_schedules(name, cl):
-    """split_combine = a cluster size: every split row's slices sit in one cluster, in key
-    order, the row's slices lengthened until there are at most `cl` of them; no merges."""
-    w = W.make(name) if name != "wide_group_d64" else W.custom("g8", [3000, 17, 700, 1, 0, 260], 16, 16, 2, 64,
-                                                                "fp16", 512, seed=9)
-    sc = schedule(w, split_combine=cl)
-    check_schedule(w, sc)
-    info = sc["info"]
-    assert info["cluster"] == cl and info["max_splits_used"] <= cl and info["num_merge_tasks"] == 0
-    base = schedule(w)["info"]
-    assert info["split_tokens"] >= base["split_tokens"]
-
-
-def test_cluster_combine_packs_rows_and_fills_holes():
-    """Rows of 3 slices share clusters of 8 (two each), single-slice rows fill the rest,
-    and only the last cluster carries padding."""
-    w = W.custom("pack", [3 * 256] * 6 + [100] * 10, 16, 8, 1, 128, "bf16", 1024, seed=2)
-    sc = schedule(w, split_combine=8, split_tokens=256)
-    check_schedule(w, sc)
-    sl = sc["slices"]
-    pad = np.flatnonzero(sl["q_row"] < 0)
-    assert len(sl) == 32 and len(pad) == 32 - 28
-    assert np.all(pad >= 24), "padding only in the last cluster"
-
-
-def test_cluster_combine_not_for_prefill_calls():
-    w = W.make("ragged")
-    sc = schedule(w, split_combine=8)
-    check_schedule(w, sc)
-    assert sc["info"]["cluster"] == 0 and sc["info"]["num_merge_tasks"] > 0
-
-
-@pytest.mark.parametrize("opts,status", [({"split_combine": 3}, "PGQA_ERR_INVALID_ARG"),
-                                         ({"split_combine": 32}, "PGQA_ERR_INVALID_ARG"),
-                                         ({"split_combine": 8, "decode_kernel": "cuda_core"}, "PGQA_ERR_UNSUPPORTED"),
-                                         ({"split_combine": 8, "pipeline_stages": 1}, "PGQA_ERR_UNSUPPORTED")])
-def test_cluster_combine_config_errors(opts, status):
-    w = W.make("qwen15_mixed")  # head_dim 128
-    with pytest.raises(pg.PagedGQAError) as e:
-        schedule(w, **opts)
-    assert e.value.name == status
-    g16 = W.custom("g16", [100], 16, 16, 1, 64, "bf16", 16, seed=1)
-    with pytest.raises(pg.PagedGQAError) as e:
-        schedule(g16, split_combine=8)
-    assert e.value.name == "PGQA_ERR_UNSUPPORTED"
