@@ -93,6 +93,31 @@ def test_multi_row_requests(causal, kernel):
     H.compare(out, lse, ro, rl, f"ragged causal={causal}")
 
 
+@pytest.mark.parametrize("head_dim,n,kernel", [(64, 20000, "tensor_core"), (128, 12000, "tensor_core"),
+                                                (128, 9000, "cuda_core")])
+def test_block_merge_long_slice_lists(head_dim, n, kernel):
+    """One-tile slices of one long row: 500-750 slices per (row, kv head), beyond the
+    block merge's up-front requests (256 per thread group), so its loop over the rest runs;
+    an empty row and a short one ride along."""
+    tile = 32 if head_dim == 64 else 16
+    w = W.custom("longlist", [n, 0, 40], 64, 8, 2, head_dim, "bf16", n // 64 + 16, seed=n + head_dim)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, info = H.gpu_outputs(w, split_tokens=tile, decode_kernel=kernel)
+    assert info["max_splits_used"] > 256
+    H.compare(out, lse, ro, rl, f"{info['max_splits_used']} slices d{head_dim} {kernel}")
+
+
+def test_many_short_rows():
+    """4096 decode rows of 0-64 keys: a grid of 8192 unsplit CTAs, many waves deep."""
+    rng = np.random.default_rng(3)
+    lens = [int(x) for x in rng.integers(0, 65, 4096)]
+    w = W.custom("many", lens, 16, 14, 2, 64, "bf16", sum(-(-n // 16) for n in lens) + 16, seed=5)
+    ro, rl = H.oracle_outputs(w)
+    out, lse, info = H.gpu_outputs(w)
+    assert info["num_items"] == 8192 and info["num_merge_tasks"] == 0
+    H.compare(out, lse, ro, rl, "4096 short rows")
+
+
 def test_explicit_scale():
     import oracle
     import paged_kv_gqa_05_gb300 as pg
