@@ -693,7 +693,8 @@ def main(argv=None):
     ap.add_argument("--max-splits", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--decode-kernel", choices=["auto", "tensor_core", "cuda_core"], default="auto")
-    ap.add_argument("--stages", type=int, default=0, choices=[0, 2, 3], help="pipeline stages per warp")
+    ap.add_argument("--stages", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="pipeline stages per warp (1: the wide form)")
     ap.add_argument("--append-mode", choices=["fused", "separate"], default="fused",
                     help="fused: pgqa_append_run per layer; separate: pgqa_kv_append then pgqa_run")
     ap.add_argument("--prefill-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto")
