@@ -548,7 +548,8 @@ static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items
 // `slots` items: each wave takes max(its bytes / rate(CTAs in it), its longest slice /
 // one CTA's rate), plus kWaveCostNs; splitting adds kMergeCostNs.
 static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_rows, int64_t longest,
-                            bool with_prefill) {
+                            int64_t prefill_ctas) {
+    const bool with_prefill = prefill_ctas > 0;
     const pgqa_plan_config &c = plan->cfg;
     const int64_t tile = plan->tile;
     const int64_t min_split = static_cast<int64_t>(kDecodeWarps) * tile;
@@ -596,7 +597,10 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
         }
         const int stages =
             c.pipeline_stages != 0 ? c.pipeline_stages : pick_stages(plan, max_slice, n_items, with_prefill);
-        const int64_t slots = static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[stages];
+        // A prefill CTA beside decode rows leaves its SM room for one decode CTA fewer
+        // (its ~104 KB of shared memory), so those slots are not the decode rows'.
+        const int64_t slots = std::max<int64_t>(
+            plan->num_sms, static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[stages] - prefill_ctas);
         if (have && (n_items > 8 * slots || n_items > plan->max_items)) break;
         const double cr = cta_rate(c.head_dim, plan->group, stages);
         std::sort(slices.begin(), slices.end(), std::greater<std::pair<int64_t, int64_t>>());
@@ -738,12 +742,33 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
         }
     }
 
+    // Prefill key slices (each >= 256 keys, at most 8), partials merged per (row, kv head)
+    // like split decode rows.  Alone, a chunk takes the most slices that still fit one wave
+    // of two CTAs per SM.  Beside decode rows it takes about one CTA per SM, leaving each
+    // SM room for decode CTAs: measured on GB300 for a 512-row chunk over 1536 keys with
+    // 127 decode rows, 2 slices (112 prefill CTAs) ran the call in 35.2 us against 41.3
+    // with 5 (280 CTAs, which filled every slot until they finished); 3 and 4 gave 36.6
+    // and 38.1.
+    int pf_splits = 1;
+    if (!prefill.empty()) {
+        int64_t kmax = 0;
+        for (const PrefillItem &t : prefill) kmax = std::max<int64_t>(kmax, t.key_end);
+        const int64_t ctas_per_sm = rowv.empty() ? 2 : 1;  // decode rows give at least one item each
+        if (c.prefill_splits > 0)
+            pf_splits = std::min(8, c.prefill_splits);
+        else
+            pf_splits = static_cast<int>(std::min<int64_t>(
+                {8, std::max<int64_t>(1, ctas_per_sm * plan->num_sms / static_cast<int64_t>(prefill.size())),
+                 std::max<int64_t>(1, kmax / 256)}));
+    }
+
     const int tile = plan->tile;
     int64_t longest = 0;
     for (const Row &rw : rowv) longest = std::max<int64_t>(longest, rw.n);
-    const int64_t ls = c.split_tokens > 0 ? round_up(c.split_tokens, tile)
-                                          : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest,
-                                                         !prefill.empty());
+    const int64_t ls = c.split_tokens > 0
+                           ? round_up(c.split_tokens, tile)
+                           : choose_slice(plan, rowv.data(), static_cast<int64_t>(rowv.size()), longest,
+                                          static_cast<int64_t>(prefill.size()) * pf_splits);
 
     std::vector<WorkItem> items;
     std::vector<MergeTask> tasks;
@@ -781,25 +806,7 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
         return (a.tok_end - a.tok_begin) > (b.tok_end - b.tok_begin);
     });
 
-    // Prefill key slices (each >= 256 keys, at most 8), partials merged per (row, kv head)
-    // like split decode rows.  Alone, a chunk takes the most slices that still fit one wave
-    // of two CTAs per SM.  Beside decode rows it takes about one CTA per SM, leaving each
-    // SM room for decode CTAs: measured on GB300 for a 512-row chunk over 1536 keys with
-    // 127 decode rows, 2 slices (112 prefill CTAs) ran the call in 35.2 us against 41.3
-    // with 5 (280 CTAs, which filled every slot until they finished); 3 and 4 gave 36.6
-    // and 38.1.
-    int pf_splits = 1;
-    if (!prefill.empty()) {
-        int64_t kmax = 0;
-        for (const PrefillItem &t : prefill) kmax = std::max<int64_t>(kmax, t.key_end);
-        const int64_t ctas_per_sm = items.empty() ? 2 : 1;
-        if (c.prefill_splits > 0)
-            pf_splits = std::min(8, c.prefill_splits);
-        else
-            pf_splits = static_cast<int>(std::min<int64_t>(
-                {8, std::max<int64_t>(1, ctas_per_sm * plan->num_sms / static_cast<int64_t>(prefill.size())),
-                 std::max<int64_t>(1, kmax / 256)}));
-    }
+    // The prefill key slices chosen above, each tile cut into pf_splits CTAs.
     if (pf_splits > 1) {
         // partial slots per (request, kv head): rows x splits, after the decode slots
         std::vector<PrefillItem> split_items;
