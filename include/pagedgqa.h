@@ -108,7 +108,11 @@ PGQA_API pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_page
  * AttentionBackend ABC with plan() / run(); design bullets: metadata in
  * persistent device buffers updated in place each step).  A plan owns device
  * buffers sized once at creation (work list, merge list, split partials), so
- * their addresses never change and run() can be captured in a CUDA graph.
+ * their addresses never change and run() can be captured in a CUDA graph.  A
+ * captured run() also fixes its launch sizes and kernel variants (the counts of
+ * slices, merges and prefill tiles and the pipeline depth that
+ * pgqa_plan_get_info reports): replay it after a pgqa_plan_update only when
+ * those are unchanged, and capture again otherwise.
  */
 typedef struct pgqa_plan pgqa_plan;
 
