@@ -110,9 +110,9 @@ PGQA_API pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_page
  * buffers sized once at creation (work list, merge list, split partials), so
  * their addresses never change and run() can be captured in a CUDA graph.  A
  * captured run() also fixes its launch sizes and kernel variants (the counts of
- * slices, merges and prefill tiles and the pipeline depth that
- * pgqa_plan_get_info reports): replay it after a pgqa_plan_update only when
- * those are unchanged, and capture again otherwise.
+ * slices, merges and prefill tiles, which pgqa_plan_get_info reports, and the
+ * pipeline depth): replay it after a pgqa_plan_update only when the update
+ * describes the same schedule, and capture again otherwise.
  */
 typedef struct pgqa_plan pgqa_plan;
 
