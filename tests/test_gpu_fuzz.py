@@ -5,8 +5,9 @@ Each case draws a shape (head_dim, page size, dtype, kv heads, group width), a b
 non-causal query rows) and plan options (slice length, split cap, pipeline depth or
 the wide form, decode and prefill kernels, prefill key slices), then runs the call
 through the C ABI -- with the step's new rows appended in the same launch when the
-draw asks for it -- and compares every output element and log-sum-exp with the
-oracle, and the appended pool rows bit for bit.  The draws cover combinations the
+draw asks for it, some of them with the rotary embedding -- and compares every output
+element and log-sum-exp with the oracle, and the appended pool rows bit for bit (the
+rotated K rows within the fp32 rotation's rounding bound).  The draws cover combinations the
 targeted tests do not enumerate.
 """
 import numpy as np
@@ -17,6 +18,7 @@ import oracle
 import paged_kv_gqa_05_gb300 as pg
 from paged_kv_gqa_05_gb300 import workloads as W
 import gpu_helpers as H
+import test_gpu_rope as R
 
 pytestmark = pytest.mark.gpu
 
@@ -59,8 +61,10 @@ def draw(seed):
         opts["prefill_splits"] = int(rng.integers(0, 5))
     fused = kernel == "tensor_core" and rng.random() < 0.4 and all(q <= n for q, n in zip(qo or [1] * batch, lens))
     out_dtype = "native" if rng.random() < 0.3 else "fp32"
+    seed = int(rng.integers(1 << 30))
+    rope = fused and bool(rng.random() < 0.5)  # the fused call with the rotary embedding
     return dict(head_dim=head_dim, page_size=page_size, dtype=dtype, hkv=hkv, group=group, lens=lens, qo=qo,
-                causal=causal, opts=opts, fused=fused, out_dtype=out_dtype, seed=int(rng.integers(1 << 30)))
+                causal=causal, opts=opts, fused=fused, out_dtype=out_dtype, seed=seed, rope=rope)
 
 
 @pytest.mark.parametrize("seed", range(160))
@@ -73,6 +77,9 @@ def test_random_call(seed):
     what = f"fuzz {seed}: {d}"
     if d["fused"]:
         H.new_rows_for_query_rows(w, seed=seed)
+    if d["rope"]:  # q and the new K rows turned at their positions; K pool rows within the rounding bound
+        R.check_fused(w, what, **d["opts"])
+        return
     ro, rl = H.oracle_outputs(w)
     native = W.TORCH_DTYPES[w.dtype]
     out_dt = native if d["out_dtype"] == "native" else torch.float32
