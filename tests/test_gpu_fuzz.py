@@ -4,11 +4,11 @@ Each case draws a shape (head_dim, page size, dtype, kv heads, group width), a b
 (lengths from empty to a few thousand keys, some requests with several causal or
 non-causal query rows) and plan options (slice length, split cap, pipeline depth or
 the wide form, decode and prefill kernels, prefill key slices), then runs the call
-through the C ABI -- with the step's new rows appended in the same launch when the
-draw asks for it, some of them with the rotary embedding -- and compares every output
-element and log-sum-exp with the oracle, and the appended pool rows bit for bit (the
-rotated K rows within the fp32 rotation's rounding bound).  The draws cover combinations the
-targeted tests do not enumerate.
+through the C ABI and compares every output element and log-sum-exp with the oracle.
+Some draws append the step's new rows: inside the call (some of those with the rotary
+embedding, the rotated K rows then held to the fp32 rotation's rounding bound, the
+other appended rows bit for bit) or by a separate append before it.  The draws cover
+combinations the targeted tests do not enumerate.
 """
 import numpy as np
 import pytest
@@ -63,8 +63,10 @@ def draw(seed):
     out_dtype = "native" if rng.random() < 0.3 else "fp32"
     seed = int(rng.integers(1 << 30))
     rope = fused and bool(rng.random() < 0.5)  # the fused call with the rotary embedding
+    # new rows appended by pgqa_kv_append before the call instead of inside it
+    separate = (not fused and bool(rng.random() < 0.3) and all(q <= n for q, n in zip(qo or [1] * batch, lens)))
     return dict(head_dim=head_dim, page_size=page_size, dtype=dtype, hkv=hkv, group=group, lens=lens, qo=qo,
-                causal=causal, opts=opts, fused=fused, out_dtype=out_dtype, seed=seed, rope=rope)
+                causal=causal, opts=opts, fused=fused, out_dtype=out_dtype, seed=seed, rope=rope, separate=separate)
 
 
 @pytest.mark.parametrize("seed", range(160))
@@ -75,7 +77,7 @@ def test_random_call(seed):
     w = W.custom(f"fuzz{seed}", d["lens"], d["page_size"], hq, d["hkv"], d["head_dim"], d["dtype"], pages,
                  seed=d["seed"], qo_lens=d["qo"], causal=d["causal"])
     what = f"fuzz {seed}: {d}"
-    if d["fused"]:
+    if d["fused"] or d["separate"]:
         H.new_rows_for_query_rows(w, seed=seed)
     if d["rope"]:  # q and the new K rows turned at their positions; K pool rows within the rounding bound
         R.check_fused(w, what, **d["opts"])
@@ -85,7 +87,7 @@ def test_random_call(seed):
     out_dt = native if d["out_dtype"] == "native" else torch.float32
     pg.read_device_flags(clear=True)
     if not d["fused"]:
-        out, lse, _ = H.gpu_outputs(w, out_dt, append=False, **d["opts"])
+        out, lse, _ = H.gpu_outputs(w, out_dt, append=d["separate"], **d["opts"])
     else:
         dev = H.to_device(w)
         plan = pg.Plan(hq, d["hkv"], d["head_dim"], d["page_size"], native, max_batch=w.batch,
