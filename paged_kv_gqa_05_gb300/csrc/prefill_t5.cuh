@@ -199,31 +199,39 @@ __global__ void __launch_bounds__(T5Cfg<D>::NTHREADS, 2)
     if (!p.prefetch_pool && copier && lane == 0)
         for (int kt = 0; kt < pre; ++kt) issue(kt);
 
-    // ---- Q: the pair rows into the swizzled K-major tile (zeros for no pair).  Each of the
-    // two threads of a pair takes chunks c and c + CH/2 (rotate-half partners) for its
-    // quarter of c in [0, CH/2).
+    // ---- Q: the pair rows into the swizzled K-major tile (zeros for no pair).  Four
+    // threads share a row, each taking chunks c and c + CH/2 (rotate-half partners) for
+    // its c in [0, CH/2) with c = its lane mod 4 (+ 4 at head_dim 128), so that every
+    // load instruction reads whole 32-byte sectors of 8 rows; 64 rows per pass, two passes.
     if (warp < C::NT / 32) {
-        constexpr int CQ = CH / 4;  // first-half chunks per thread
-        const T *qrow = static_cast<const T *>(p.q) +
-                        (static_cast<size_t>(it.q_row0 + (valid ? qi : 0)) * p.num_qo_heads + it.kv_head * G +
-                         (valid ? qh : 0)) * D;
+        constexpr int CQ = CH / 8;  // first-half chunks per thread and row
 #pragma unroll
-        for (int u = 0; u < CQ; ++u) {
-            const int c = half * CQ + u;
-            uint4 lo4 = valid ? __ldg(reinterpret_cast<const uint4 *>(qrow + c * 8)) : make_uint4(0u, 0u, 0u, 0u);
-            uint4 hi4 =
-                valid ? __ldg(reinterpret_cast<const uint4 *>(qrow + (c + CH / 2) * 8)) : make_uint4(0u, 0u, 0u, 0u);
-            if (ROPE && valid) {
-                const float2 *cs = p.rope_cs + static_cast<size_t>(new_begin + qi) * (D / 2);
-                uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+        for (int pass = 0; pass < C::MP / 64; ++pass) {
+            const int r = pass * 64 + (tid >> 2);  // the pair row within the CTA
+            const int rm = it.pair0 + r;
+            const int ri = rm / G, rh = rm - (rm / G) * G;
+            const bool rvalid = ri < it.rows;
+            const T *qrow = static_cast<const T *>(p.q) +
+                            (static_cast<size_t>(it.q_row0 + (rvalid ? ri : 0)) * p.num_qo_heads + it.kv_head * G +
+                             (rvalid ? rh : 0)) * D;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    rope_rotate2<T>(lo[j], hi[j], __ldg(reinterpret_cast<const float4 *>(cs + 8 * c + 2 * j)));
-                lo4 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                hi4 = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            for (int u = 0; u < CQ; ++u) {
+                const int c = (tid & 3) + 4 * u;
+                uint4 lo4 = rvalid ? __ldg(reinterpret_cast<const uint4 *>(qrow + c * 8)) : make_uint4(0u, 0u, 0u, 0u);
+                uint4 hi4 = rvalid ? __ldg(reinterpret_cast<const uint4 *>(qrow + (c + CH / 2) * 8))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                if (ROPE && rvalid) {
+                    const float2 *cs = p.rope_cs + static_cast<size_t>(new_begin + ri) * (D / 2);
+                    uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        rope_rotate2<T>(lo[j], hi[j], __ldg(reinterpret_cast<const float4 *>(cs + 8 * c + 2 * j)));
+                    lo4 = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    hi4 = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                *reinterpret_cast<uint4 *>(qs + swz_off(r, c, C::QHALF_BYTES)) = lo4;
+                *reinterpret_cast<uint4 *>(qs + swz_off(r, c + CH / 2, C::QHALF_BYTES)) = hi4;
             }
-            *reinterpret_cast<uint4 *>(qs + swz_off(prow, c, C::QHALF_BYTES)) = lo4;
-            *reinterpret_cast<uint4 *>(qs + swz_off(prow, c + CH / 2, C::QHALF_BYTES)) = hi4;
         }
     }
     fence_proxy_async_smem();  // generic stores before the products read the tile
