@@ -285,6 +285,12 @@ __device__ __forceinline__ SlicePages stage_slice_pages(int32_t *buf, const int3
     return sp;  // caller synchronises the CTA before use
 }
 
+// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -218,6 +218,14 @@ __global__ void __launch_bounds__(NW * 32, (STAGES == 2 && NH == 1 && NW == kDec
     // path by which a CTA reports a stuck pipeline instead of hanging.  Nothing is in
     // flight into that stage, and the other stages' copies are drained as usual.
     const bool stall = p.stall_wait_us != 0 && warp == 0;
+    // The group's q rows are requested into L2 before the dependency wait.  It is only a
+    // hint: should the grid before this one write q, its stores land in L2 as well, and
+    // the loads after the wait read them there.  (Timed on GB300: 32 mixed rows 13.97 ->
+    // 13.73 us per call, 1 x 32k 10.89 -> 10.79; the 128 x 301 step unchanged.)
+    if (threadIdx.x == 0) {
+        const T *qg = static_cast<const T *>(p.q) + (static_cast<size_t>(it.q_row) * p.num_qo_heads + it.kv_head * G) * D;
+        prefetch_l2_bulk(qg, static_cast<uint32_t>(G * D * sizeof(T)));
+    }
     // K/V loads start before the grid-dependency wait when the caller has stated
     // that nothing still in flight writes the pool rows this call reads.
     const int pre = my_tiles < C::ST ? my_tiles : C::ST;
