@@ -13,6 +13,8 @@
 // is read with many independent coalesced loads in flight.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace pgqa {
@@ -49,6 +51,30 @@ __device__ __forceinline__ void put<__nv_bfloat16>(void *out, size_t i, float v)
 template <>
 __device__ __forceinline__ void put<__half>(void *out, size_t i, float v) {
     static_cast<__half *>(out)[i] = __float2half_rn(v);
+}
+
+// V consecutive outputs of one lane (V = 2 or 4, oi a multiple of V) as one store.
+template <typename OutT, int V>
+__device__ __forceinline__ void put_row(void *out, size_t oi, const float (&v)[V]) {
+    if constexpr (std::is_same<OutT, float>::value) {
+        if constexpr (V == 4)
+            *reinterpret_cast<float4 *>(static_cast<float *>(out) + oi) = make_float4(v[0], v[1], v[2], v[3]);
+        else
+            *reinterpret_cast<float2 *>(static_cast<float *>(out) + oi) = make_float2(v[0], v[1]);
+    } else {
+        uint32_t w[V / 2];
+#pragma unroll
+        for (int j = 0; j < V / 2; ++j) {
+            OutT pair[2];
+            put<OutT>(pair, 0, v[2 * j]);
+            put<OutT>(pair, 1, v[2 * j + 1]);
+            w[j] = *reinterpret_cast<const uint32_t *>(pair);
+        }
+        if constexpr (V == 4)
+            *reinterpret_cast<uint2 *>(static_cast<OutT *>(out) + oi) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t *>(static_cast<OutT *>(out) + oi) = w[0];
+    }
 }
 
 template <typename OutT>
@@ -212,7 +238,8 @@ __global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, in
     const int head = t.kv_head * G + h;
     const size_t oi = (static_cast<size_t>(t.q_row) * p.num_qo_heads + head) * D + lane * V;
 #pragma unroll
-    for (int j = 0; j < V; ++j) put<OutT>(p.out, oi + j, sum == 0.f ? 0.f : acc[j] / sum);
+    for (int j = 0; j < V; ++j) acc[j] = sum == 0.f ? 0.f : acc[j] / sum;
+    put_row<OutT, V>(p.out, oi, acc);  // one vector store per lane
     if (lane == 0 && p.lse != nullptr)
         p.lse[static_cast<size_t>(t.q_row) * p.num_qo_heads + head] =
             sum == 0.f ? -INFINITY : (mx + log2f(sum)) * 0.6931471805599453f;
