@@ -536,7 +536,10 @@ static int pick_stages(const pgqa_plan *plan, int64_t max_slice, int64_t n_items
         return 1;
     const int64_t held = 3LL * kDecodeWarps * plan->tile;  // keys three stages hold
     if (max_slice <= held) return 3;
-    if (!with_prefill && max_slice >= 2 * held &&
+    // Long slices (a warp tile past what three stages hold) in a grid short of one full
+    // wave: SMs with one CTA have the shared memory for the deeper ring (timed on GB300
+    // for 1 x 32k: 256-key slices at three stages 9.9 us, 224-key slices at two 10.35).
+    if (!with_prefill && max_slice >= held + kDecodeWarps * plan->tile &&
         n_items < static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[3])
         return 3;
     return 2;
