@@ -322,3 +322,21 @@ def test_prefill_slices_leave_room_for_decode_rows():
     mixed = schedule(W.make("ragged"))["info"]
     assert SMS < alone["num_prefill_tiles"] <= 2 * SMS
     assert mixed["num_items"] > 0 and mixed["num_prefill_tiles"] <= SMS
+
+
+# The plan's choices for the benchmark's workloads on 152 SMs, each the best or within
+# ~1 % of the best of the forced alternatives timed on GB300 (slice length in keys,
+# pipeline depth, decode CTAs): a change to the split model shows up here first.
+BENCH_CHOICES = {
+    "qwen05_decode": (320, 1, 256),      # whole rows, the wide form
+    "qwen15_mixed": (448, 3, 292),
+    "long_context_b1": (256, 3, 256),    # 128 slices per kv head at three stages
+    "long_context_b4": (896, 3, 296),
+    "ragged": (2048, 2, 374),            # decode slots net of the 112 prefill CTAs
+}
+
+
+@pytest.mark.parametrize("name", sorted(BENCH_CHOICES))
+def test_plan_choices_for_the_benchmark_workloads(name):
+    info = schedule(W.make(name))["info"]
+    assert (info["split_tokens"], info["pipeline_stages"], info["num_items"]) == BENCH_CHOICES[name]
