@@ -168,11 +168,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 // 13.27 against 13.61 us per layer with P = 16 instead of 8; the ragged call, rows of
 // 2-3 slices, 38.0 us with P = 4, 38.2 with 8, 38.5 with 16).
 template <typename OutT, int D, int P>
-__global__ void __launch_bounds__(128) merge_warp_kernel(const MergeParams p, int units) {
+__global__ void __launch_bounds__(256) merge_warp_kernel(const MergeParams p, int units) {
     pdl_launch_dependents();
     constexpr int V = D / 32;  // channels per lane: 2 (D = 64) or 4 (D = 128)
     const int lane = threadIdx.x & 31;
-    const int u = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (u >= units) return;
     const int G = p.group;
     const MergeTask t = p.tasks[u / G];  // written by plan_update's copy only
@@ -254,8 +254,12 @@ cudaError_t launch_merge_t(const MergeParams &p, int num_tasks, int max_splits, 
     if (max_splits <= 32) {
         const int units = num_tasks * p.group;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((units + 3) / 4);
-        cfg.blockDim = dim3(128);
+        // Four warps a block, or eight for long lists of units (timed on GB300: the ragged
+        // call's ~8000 units 33.1 -> 32.8 us, the 512-row chunk's ~7200 15.1 -> 14.9; 32
+        // mixed rows, 228 units, 13.24 -> 13.33 with eight, so they keep four).
+        const int wpb = units >= 2048 ? 8 : 4;
+        cfg.gridDim = dim3((units + wpb - 1) / wpb);
+        cfg.blockDim = dim3(32 * wpb);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
