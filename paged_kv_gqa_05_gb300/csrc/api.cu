@@ -570,6 +570,8 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
     }
     std::vector<std::pair<int64_t, int64_t>> slices;  // (slice length, items)
     slices.reserve(2 * hist.size());
+    std::vector<uint64_t> order;  // slices, longest first (see below)
+    order.reserve(2 * hist.size());
     int64_t best_len = round_up(std::max<int64_t>(longest, min_split), tile), prev_len = -1;
     double best = 0.0;
     bool have = false;
@@ -606,7 +608,13 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
             plan->num_sms, static_cast<int64_t>(plan->num_sms) * plan->slots_per_sm[stages] - prefill_ctas);
         if (have && (n_items > 8 * slots || n_items > plan->max_items)) break;
         const double cr = cta_rate(c.head_dim, plan->group, stages);
-        std::sort(slices.begin(), slices.end(), std::greater<std::pair<int64_t, int64_t>>());
+        // Longest slices first: sort packed keys (length, then the entry's index, which only
+        // orders slices of equal length, and those are interchangeable in the walk below) --
+        // a fraction of the cost of sorting the pairs, which dominated plan_update's host time.
+        order.resize(slices.size());
+        for (size_t i = 0; i < slices.size(); ++i)
+            order[i] = (static_cast<uint64_t>(slices[i].first) << 33) | static_cast<uint64_t>(i);
+        std::sort(order.begin(), order.end(), std::greater<uint64_t>());
         double t = 0.0, wave_bytes = 0.0;
         int64_t free_slots = slots, in_wave = 0, first = -1;
         auto close_wave = [&]() {
@@ -614,7 +622,8 @@ static int64_t choose_slice(const pgqa_plan *plan, const Row *rows, int64_t n_ro
             const double rate = nc / std::cbrt(1.0 + std::pow(nc / kSaturatedRate, 3.0));
             t += std::max(wave_bytes / rate, static_cast<double>(first) * row_bytes / cr) + kWaveCostNs;
         };
-        for (const auto &sl : slices) {
+        for (const uint64_t key : order) {
+            const auto &sl = slices[key & ((uint64_t(1) << 33) - 1)];
             int64_t cnt = sl.second;
             while (cnt > 0) {
                 const int64_t take = std::min(cnt, free_slots);
