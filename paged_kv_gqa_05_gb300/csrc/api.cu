@@ -519,12 +519,12 @@ static constexpr double kMergeCostNs = 2000.0;    // the merge launch, once any 
 // Pipeline depth of the tensor-core decode kernel: three stages when every warp's tiles
 // of the longest slice can be requested at once (the whole slice in flight from the
 // start), or when the grid is less than one full wave at two CTAs per SM (so some SMs
-// run a single CTA), its slices are long (at least twice what three stages hold) and no
-// prefill grid shares the GPU.  Measured on GB300: 32 mixed d 128 (292 CTAs) -4 %,
-// 64 x 2049 at g = 16 (256 CTAs) -6 %; a full wave (4 x 32k, 304 CTAs) ran its launch 6 %
-// slower, 224-key slices (1 x 32k) lost 8 %, and a ragged call, whose decode rows then went
-// unsplit, 9 %.  Otherwise two, so that three CTAs fit on an SM and overlap each other's
-// set-up and epilogue.
+// run a single CTA), its slices are long (every warp's share at least one warp tile past
+// what its three stages hold) and no prefill grid shares the GPU.  Measured on GB300:
+// 32 mixed d 128 (292 CTAs) -4 %, 64 x 2049 at g = 16 (256 CTAs) -6 %; a full wave
+// (4 x 32k, 304 CTAs) ran its launch 6 % slower, and a ragged call, whose decode rows then
+// went unsplit, 9 %.  Otherwise two, so that three CTAs fit on an SM and overlap each
+// other's set-up and epilogue.
 //
 // Slices of at most kDecodeWideWarps warp tiles take the wide form instead (reported as
 // depth 1): one warp per tile, the whole slice requested at once, so no warp of the CTA
@@ -823,10 +823,10 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
         // partial slots per (request, kv head): rows x splits, after the decode slots
         std::vector<PrefillItem> split_items;
         split_items.reserve(prefill.size() * pf_splits);
-        int64_t prev_req_key = -1, base = 0;
+        int32_t prev_row0 = -1, prev_head = -1;
+        int64_t base = 0;
         for (const PrefillItem &t : prefill) {
-            const int64_t req_key = (static_cast<int64_t>(t.q_row0) << 8) | t.kv_head;
-            if (req_key != prev_req_key) {
+            if (t.q_row0 != prev_row0 || t.kv_head != prev_head) {  // a new (request, kv head)
                 base = slot;
                 slot += t.rows * pf_splits;
                 if (slot > plan->max_slots) return fail(PGQA_ERR_CAPACITY, "split partials exceed the plan capacity");
@@ -835,7 +835,8 @@ static pgqa_status build_schedule(const pgqa_plan *plan, const int32_t *kv_indpt
                         return fail(PGQA_ERR_CAPACITY, "merge tasks exceed the plan capacity");
                     tasks.push_back({t.q_row0 + i, t.kv_head, static_cast<int32_t>(base + i * pf_splits), pf_splits});
                 }
-                prev_req_key = req_key;
+                prev_row0 = t.q_row0;
+                prev_head = t.kv_head;
             }
             const int64_t len = round_up(ceil_div(std::max<int32_t>(1, t.key_end), pf_splits), 64);
             for (int sidx = 0; sidx < pf_splits; ++sidx) {

@@ -315,6 +315,16 @@ def test_checker_catches_broken_schedules(mistake):
         check_schedule(w, _mutants(sc)[mistake])
 
 
+def test_prefill_partials_with_many_kv_heads():
+    """Split prefill tiles get their partial slots and merges per (request, kv head) for
+    any number of kv heads: request 0 (rows 0-1) ends on kv head 512 and request 1
+    starts at row 2, kv head 0."""
+    w = W.custom("heads513", [20, 30], 16, 513, 513, 64, "bf16", 8, seed=5, qo_lens=[2, 3], causal=True)
+    sc = schedule(w, prefill_splits=2)
+    assert sc["info"]["num_prefill_tiles"] == 2 * 2 * 513
+    check_schedule(w, sc)
+
+
 def test_prefill_slices_leave_room_for_decode_rows():
     """A chunk alone takes up to two prefill CTAs per SM; beside decode rows about one, so
     that decode CTAs run next to the prefill tiles instead of waiting for them."""
