@@ -159,6 +159,7 @@ struct MapCacheEntry {
     const void *ptr = nullptr;
     int64_t num_pages = 0;
     int box_rows = 0;
+    bool swizzle128 = false;
     CUtensorMap map;
 };
 
@@ -214,7 +215,7 @@ struct pgqa_plan {
 static pgqa_status pool_map(pgqa_plan *plan, const void *pool, int box_rows, bool swizzle128,
                             const CUtensorMap **out) {
     for (auto &e : plan->maps)
-        if (e.ptr == pool && e.num_pages == plan->num_pages && e.box_rows == box_rows) {
+        if (e.ptr == pool && e.num_pages == plan->num_pages && e.box_rows == box_rows && e.swizzle128 == swizzle128) {
             *out = &e.map;
             return PGQA_OK;
         }
@@ -229,6 +230,7 @@ static pgqa_status pool_map(pgqa_plan *plan, const void *pool, int box_rows, boo
     e.ptr = pool;
     e.num_pages = plan->num_pages;
     e.box_rows = box_rows;
+    e.swizzle128 = swizzle128;
     *out = &e.map;
     return PGQA_OK;
 }
@@ -407,10 +409,11 @@ static pgqa_status plan_capacity(pgqa_plan *p) {
     p->ctas_per_sm = std::max(p->slots_per_sm[2], p->slots_per_sm[3]);
     // Slices never exceed 8 waves of CTAs + one per row and kv head; forced short slices may need more.
     const int64_t items = c.max_q_rows * c.num_kv_heads + 8LL * p->num_sms * p->ctas_per_sm + 64;
-    if (items > (1 << 26)) return fail(PGQA_ERR_CAPACITY, "plan capacity too large");
+    const int64_t prefill = (c.max_q_rows * p->group / 64 + c.max_batch + 1) * c.num_kv_heads * 8;
+    if (items > (1 << 26) || prefill > (1 << 26)) return fail(PGQA_ERR_CAPACITY, "plan capacity too large");
     p->max_items = static_cast<int>(items);
     p->max_tasks = static_cast<int>(c.max_q_rows * c.num_kv_heads);
-    p->max_prefill = static_cast<int>((c.max_q_rows * p->group / 64 + c.max_batch + 1) * c.num_kv_heads * 8);
+    p->max_prefill = static_cast<int>(prefill);
     // partial slots: split decode slices, plus up to 8 key slices per prefill row and kv head
     p->max_slots = p->max_items + static_cast<int>(c.max_q_rows * c.num_kv_heads * 8);
     return PGQA_OK;

@@ -197,6 +197,16 @@ def test_forced_short_slices_over_capacity():
     assert e.value.name == "PGQA_ERR_CAPACITY"
 
 
+@pytest.mark.parametrize("max_batch, max_q_rows", [(10 ** 8, 4), (4, 1 << 24)])
+def test_oversized_plan_is_a_capacity_error(max_batch, max_q_rows):
+    """Plans whose lists would pass 2^26 entries (the prefill tiles of 10^8 requests, the
+    work items of 2^24 rows x 4 kv heads) are refused, not sized from a wrapped count."""
+    w = W.custom("cap", [5, 9, 0, 40], 16, 8, 4, 64, "bf16", 8, seed=6)
+    with pytest.raises(B.PagedGQAError) as e:
+        schedule(w, max_batch=max_batch, max_q_rows=max_q_rows)
+    assert e.value.name == "PGQA_ERR_CAPACITY"
+
+
 def test_cuda_core_kernel_runs_prefill_rows_as_decode_rows():
     """Without tensor-core prefill tiles, every query row of a chunk is a decode row over
     its causal prefix of the keys."""
