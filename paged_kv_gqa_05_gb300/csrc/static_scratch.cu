@@ -143,7 +143,13 @@ extern "C" PGQA_API pgqa_status pgqa_decode_static_scratch(const void *q, const 
          reinterpret_cast<uintptr_t>(out)) & 15u)
         return report(PGQA_ERR_INVALID_ARG, "q, pools and out must be 16-byte aligned");
 
-    // Scratch layout: work items | merge tasks | partial outputs | partial lse.
+    // Scratch layout: work items | merge tasks | partial outputs | partial lse.  The
+    // request count is bounded first, so that the sizes below cannot wrap.
+    const uint64_t max_items = kStaticScratchBytes / sizeof(WorkItem);
+    const uint64_t pairs = static_cast<uint64_t>(batch) * static_cast<uint64_t>(num_kv_heads);  // < 2^62
+    if (pairs > max_items || pairs * static_cast<uint64_t>(splits) > max_items)
+        return report(PGQA_ERR_CAPACITY,
+                      "batch x kv heads x splits needs more than the 8 MiB static scratch; lower splits or batch");
     const size_t n_items = static_cast<size_t>(batch) * num_kv_heads * splits;
     const size_t n_tasks = static_cast<size_t>(batch) * num_kv_heads;
     const size_t items_bytes = align256(n_items * sizeof(WorkItem));

@@ -74,6 +74,13 @@ def test_argument_checks_before_device(lib):
     assert lib.pgqa_plan_create(ctypes.byref(h), ctypes.byref(PC(14, 2, 64, 16, 0, 4, 4, 0, 0, 0, 2, 0, 0,
                                                                   4096, 1.0e6))) == 2  # CUDA-core kernel
     assert lib.pgqa_kv_append_rope(None, None, None, 1, None, None, None, None, 1, None) == 1
+    # the static-scratch entry point sizes its scratch without wrapping: 2^30 requests x
+    # 2^30 kv heads x 256 slices is a capacity error (the pointers are never dereferenced)
+    ptr = 1 << 12
+    assert lib.pgqa_decode_static_scratch(ptr, ptr, ptr, ptr, None, 0, ptr, 1 << 30, 1, 16, 1 << 30, 1 << 30,
+                                          64, 0, 256, ptr, 0, None, 0.0, None) == 5
+    assert lib.pgqa_decode_static_scratch(ptr, ptr, ptr, ptr, None, 0, ptr, 1 << 30, 1, 16, 1 << 30, 1 << 30,
+                                          64, 0, 1, ptr, 0, None, 0.0, None) == 5
 
 
 def test_plan_config_layout():
