@@ -92,7 +92,8 @@ PGQA_API pgqa_status pgqa_read_device_flags(uint32_t *flags_host, int clear);
  *                   slot skips the row (padding).  A slot >= num_pages*page_size
  *                   is skipped and raises PGQA_FLAG_SLOT_RANGE.  Two rows with
  *                   the same slot in one call race (undefined which one lands).
- * The copy is bit-exact.  num_tokens == 0 enqueues nothing.
+ * num_kv_heads is 1 .. 2^20 (PGQA_ERR_UNSUPPORTED above).  The copy is
+ * bit-exact.  num_tokens == 0 enqueues nothing.
  */
 PGQA_API pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_pages, int page_size,
                            int num_kv_heads, int head_dim, pgqa_dtype dtype,

@@ -307,6 +307,7 @@ pgqa_status pgqa_kv_append(void *k_pool, void *v_pool, int64_t num_pages, int pa
     if (head_dim != 64 && head_dim != 128) return fail(PGQA_ERR_UNSUPPORTED, "head_dim %d", head_dim);
     if (!supported_page_size(page_size)) return fail(PGQA_ERR_UNSUPPORTED, "page_size %d", page_size);
     if (num_kv_heads < 1) return fail(PGQA_ERR_INVALID_ARG, "num_kv_heads %d", num_kv_heads);
+    if (num_kv_heads > (1 << 20)) return fail(PGQA_ERR_UNSUPPORTED, "num_kv_heads %d > 2^20", num_kv_heads);
     if (num_tokens == 0) return PGQA_OK;
     if (!k_pool || !v_pool || !k || !v || !slot_mapping) return fail(PGQA_ERR_INVALID_ARG, "NULL pointer");
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k) || !aligned16(v))

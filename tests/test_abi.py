@@ -63,6 +63,7 @@ def test_argument_checks_before_device(lib):
     assert lib.pgqa_kv_append(None, None, 1, 16, 2, 64, 0, None, None, None, 0, None) == 0
     assert lib.pgqa_kv_append(None, None, 1, 16, 2, 64, 0, None, None, None, 1, None) == 1
     assert lib.pgqa_kv_append(None, None, 1, 12, 2, 64, 0, None, None, None, 1, None) == 2
+    assert lib.pgqa_kv_append(None, None, 1, 16, (1 << 20) + 1, 64, 0, None, None, None, 1, None) == 2
     assert lib.pgqa_plan_update(None, None, None, None, 0, None, None, 0, 0, None) == 1
     assert lib.pgqa_run(None, None, None, None, None, 0, None, 0.0, None) == 1
     # RoPE configuration checks, also before any device call
