@@ -10,6 +10,7 @@ call raises.
 from __future__ import annotations
 
 import ctypes
+import inspect
 from pathlib import Path
 from typing import Optional
 
@@ -382,23 +383,56 @@ def read_device_flags(clear: bool = True) -> int:
     return int(v.value)
 
 
+_RUN_SIGNATURE = inspect.signature(run)
+_APPEND_RUN_SIGNATURE = inspect.signature(append_run)
+_UPDATE_SIGNATURE = inspect.signature(plan_update)
+
+
 class Plan:
-    """Owns a plan handle; plan()/run() in the style of an attention backend."""
+    """Owns a plan handle; plan()/run() in the style of an attention backend.
+
+    Unlike the module-level calls, which take a bare handle, run() and append_run()
+    here check that every tensor holds at least the elements the plan's last
+    successful update() reads or writes through it (the C ABI receives pointers
+    only and cannot), and raise ValueError before any launch otherwise."""
 
     def __init__(self, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
                  dtype: torch.dtype, max_batch: int, max_q_rows: int, **options):
         self.handle = plan_create(num_qo_heads, num_kv_heads, head_dim, page_size, dtype,
                                   max_batch, max_q_rows, **options)
+        self._shape(num_qo_heads, num_kv_heads, head_dim, page_size)
+
+    def _shape(self, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int) -> None:
         self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
+        self.page_size = page_size
+        self._num_pages = None  # pool pages of the last successful update()
+
+    def _check_sizes(self, arguments: dict) -> None:
+        if self._num_pages is None:
+            return  # no successful update: the library refuses the call itself
+        rows = int(self.info()["total_q_rows"])
+        hq, hkv, d = self.num_qo_heads, self.num_kv_heads, self.head_dim
+        pool = self._num_pages * self.page_size * hkv * d
+        need = {"q": rows * hq * d, "out": rows * hq * d, "lse": rows * hq, "k_pool": pool, "v_pool": pool,
+                "k_new": rows * hkv * d, "v_new": rows * hkv * d}
+        for name, n in need.items():
+            t = arguments.get(name)
+            if isinstance(t, torch.Tensor) and t.numel() < n:
+                raise ValueError(f"{name} holds {t.numel()} elements; the plan reads or writes {n} "
+                                 f"({rows} query rows, {self._num_pages} pool pages)")
 
     def update(self, *args, **kwargs) -> "Plan":
+        self._num_pages = None
         plan_update(self.handle, *args, **kwargs)
+        self._num_pages = int(_UPDATE_SIGNATURE.bind(self.handle, *args, **kwargs).arguments["num_pages"])
         return self
 
     def run(self, *args, **kwargs) -> torch.Tensor:
+        self._check_sizes(_RUN_SIGNATURE.bind(self.handle, *args, **kwargs).arguments)
         return run(self.handle, *args, **kwargs)
 
     def append_run(self, *args, **kwargs) -> torch.Tensor:
+        self._check_sizes(_APPEND_RUN_SIGNATURE.bind(self.handle, *args, **kwargs).arguments)
         return append_run(self.handle, *args, **kwargs)
 
     def kv_append_rope(self, *args, **kwargs) -> None:
