@@ -5,6 +5,7 @@ on exactly one CTA, and tile every prefill request's (row, head) pairs and causa
 range; malformed tables fail with the statuses plan_update gives."""
 import ctypes
 from collections import defaultdict
+from types import SimpleNamespace
 
 import numpy as np
 import pytest
@@ -224,6 +225,65 @@ def test_edge_tables(causal, head_dim):
                  qo_lens=[1, 1, 1, 4, 6, 1, 2], causal=causal)
     for opts in ({}, {"split_tokens": 16}, {"prefill_splits": 3}):
         check_schedule(w, schedule(w, **opts))
+
+
+def random_table(seed):
+    """A seeded page table with the schedule options to plan it under: uniform, equal,
+    short and heavy-tailed key counts (empty requests included), some multi-row causal or
+    non-causal requests, head shapes, page sizes, split caps, forced prefill key slices,
+    slot counts, both kernels and SM counts."""
+    rng = np.random.default_rng(5000 + seed)
+    hd, ps = int(rng.choice([64, 128])), int(rng.choice([16, 32, 64, 128, 256]))
+    hkv, g = int(rng.choice([1, 2, 4, 8])), int(rng.choice([1, 2, 4, 7, 8, 12, 16]))
+    batch = int(rng.integers(1, 96))
+    mode = rng.random()
+    if mode < 0.3:
+        lens = rng.integers(0, 5000, batch)
+    elif mode < 0.5:
+        lens = np.full(batch, int(rng.integers(1, 40000)))
+    elif mode < 0.7:
+        lens = rng.integers(0, 300, batch)
+    else:
+        lens = (rng.pareto(1.2, batch) * 500).astype(np.int64).clip(0, 60000)
+    qo = None
+    if rng.random() < 0.4:
+        q = np.ones(batch, np.int64)
+        for b in rng.choice(batch, size=max(1, batch // 8), replace=False):
+            q[b] = int(rng.integers(2, max(3, min(int(lens[b]) + 4, 700))))
+        qo = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+    npg = np.where(lens > 0, -(-lens // ps), 0)
+    indptr = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    num_pages = int(indptr[-1]) + 4
+    opts = {}
+    r = rng.random()
+    if r < 0.15:
+        opts["max_splits"] = int(rng.integers(1, 6))
+    elif r < 0.3:
+        opts["prefill_splits"] = int(rng.integers(1, 9))
+    if rng.random() < 0.2:
+        opts["ctas_per_sm"] = int(rng.integers(1, 4))
+    if g <= 8 and rng.random() < 0.1:
+        opts["decode_kernel"] = "cuda_core"
+    elif rng.random() < 0.2:
+        opts["prefill_kernel"] = "mma_sync"
+    w = SimpleNamespace(
+        num_qo_heads=g * hkv, num_kv_heads=hkv, head_dim=hd, page_size=ps,
+        dtype=str(rng.choice(["bf16", "fp16"])), batch=batch, kv_lens=lens.astype(np.int64),
+        kv_indptr=indptr, last_page_len=np.where(lens > 0, lens - (npg - 1) * ps, 0).astype(np.int32),
+        kv_indices=rng.permutation(num_pages)[: indptr[-1]].astype(np.int32), num_pages=num_pages,
+        qo_indptr=qo, causal=qo is not None and bool(rng.random() < 0.7))
+    rows = batch if qo is None else int(qo[-1])
+    return w, dict(opts, max_q_rows=rows, num_sms=int(rng.choice([152, 148, 132, 76]))), opts
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_tables(seed):
+    """Every invariant of the schedule on seeded random tables and options."""
+    w, args, opts = random_table(seed)
+    sc = schedule(w, **args)
+    check_schedule(w, sc, prefill_rows_on_tiles=opts.get("decode_kernel") != "cuda_core")
+    if opts.get("max_splits"):
+        assert sc["info"]["max_splits_used"] <= opts["max_splits"]
 
 
 def test_table_errors_match_plan_update():
