@@ -191,7 +191,9 @@ typedef struct pgqa_plan_config {
 /*
  * Creates a plan on the current device.  Allocates its device and pinned host
  * buffers (the only allocations the library makes) and, for a RoPE plan, builds
- * its rotary table (synchronously).  *plan is set to NULL on failure.
+ * its rotary table (synchronously).  *plan is set to NULL on failure.  Its lists
+ * are sized from max_q_rows, max_batch and num_kv_heads; a plan whose work list
+ * or prefill-tile list would pass 2^26 entries is refused (PGQA_ERR_CAPACITY).
  */
 PGQA_API pgqa_status pgqa_plan_create(pgqa_plan **plan, const pgqa_plan_config *cfg);
 
