@@ -152,13 +152,23 @@ def _dev(t: torch.Tensor, name: str) -> int:
 
 
 def _host_i32(a, name: str) -> Optional[np.ndarray]:
+    """A host int32 copy (or view) of an integer array; values that int32 cannot hold
+    and non-integer arrays raise instead of being truncated."""
     if a is None:
         return None
     if isinstance(a, torch.Tensor):
         if a.is_cuda:
             raise ValueError(f"{name} must be a host array")
         a = a.numpy()
-    return np.ascontiguousarray(a, dtype=np.int32)
+    arr = np.asarray(a)
+    if arr.size:
+        if arr.dtype.kind not in "iu":
+            raise ValueError(f"{name} must hold integers, not {arr.dtype}")
+        if arr.dtype.itemsize > 4 or arr.dtype == np.uint32:
+            lo, hi = int(arr.min()), int(arr.max())
+            if lo < -(1 << 31) or hi >= (1 << 31):
+                raise ValueError(f"{name} holds values outside int32 ({lo} .. {hi})")
+    return np.ascontiguousarray(arr, dtype=np.int32)
 
 
 def _i32ptr(a: Optional[np.ndarray]):

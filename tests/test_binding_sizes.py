@@ -1,6 +1,8 @@
-"""CPU checks of the Python Plan's tensor-size checks, with the library calls replaced
-by recorders: Plan.run and Plan.append_run refuse tensors smaller than what the plan's
-last successful update reads or writes through them, before anything is launched."""
+"""CPU checks of the binding's argument checks.  With the library calls replaced by
+recorders: Plan.run and Plan.append_run refuse tensors smaller than what the plan's
+last successful update reads or writes through them, before anything is launched.
+Through pgqa_plan_schedule: host page-table arrays are converted to int32 only when
+every value fits."""
 import pytest
 import torch
 
@@ -85,3 +87,17 @@ def test_failed_update_turns_the_checks_off(plan, monkeypatch):
     k, v = pools(1)
     plan.run(t(1, HQ, D), k, v)  # passed on: the library reports the plan as not updated
     assert plan.calls[-1][0] == "run"
+
+
+@pytest.mark.parametrize("bad", [[0, 1 << 31], [-(1 << 31) - 1], [0.5, 1.0], [True, False]])
+def test_host_tables_are_not_truncated(bad):
+    """Page-table arrays that int32 cannot hold exactly are refused, not wrapped."""
+    with pytest.raises(ValueError):
+        B.plan_schedule(4, 2, 64, 16, torch.bfloat16, bad, [1], [0], 4)
+
+
+def test_host_tables_accept_any_integer_type():
+    import numpy as np
+    for a in ([0, 1], np.array([0, 1], np.int64), torch.tensor([0, 1]), np.array([0, 1], np.uint16)):
+        s = B.plan_schedule(4, 2, 64, 16, torch.bfloat16, a, [5], [0], 4)
+        assert s["info"]["num_items"] == 2
