@@ -189,6 +189,8 @@ def kv_append(k_pool: torch.Tensor, v_pool: torch.Tensor, k: torch.Tensor, v: to
         raise ValueError("pools and rows must share one dtype")
     if slot_mapping.dtype != torch.int64:
         raise ValueError("slot_mapping must be int64")
+    if slot_mapping.numel() < k.shape[0]:
+        raise ValueError("slot_mapping needs one slot per row")
     lib = load()
     _check(lib.pgqa_kv_append(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), P, ps, Hkv, D,
                               TORCH_TO_CODE[k.dtype], _dev(k, "k"), _dev(v, "v"),

@@ -101,3 +101,10 @@ def test_host_tables_accept_any_integer_type():
     for a in ([0, 1], np.array([0, 1], np.int64), torch.tensor([0, 1]), np.array([0, 1], np.uint16)):
         s = B.plan_schedule(4, 2, 64, 16, torch.bfloat16, a, [5], [0], 4)
         assert s["info"]["num_items"] == 2
+
+
+def test_append_needs_a_slot_per_row():
+    k = torch.zeros(3, HKV, D, dtype=torch.bfloat16)
+    kp, vp = pools()
+    with pytest.raises(ValueError, match="one slot per row"):
+        B.kv_append(kp, vp, k, k, torch.zeros(2, dtype=torch.int64))
