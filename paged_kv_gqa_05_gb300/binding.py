@@ -325,6 +325,11 @@ def decode_static_scratch(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
         if t.dtype != torch.int32:
             raise ValueError(f"{name} must be int32")
     P, ps, Hkv, D = k_pool.shape
+    batch, hq = q.shape[0], q.shape[1]
+    for t, n, name in ((kv_indptr, batch + 1, "kv_indptr"), (last_page_len, batch, "last_page_len"),
+                       (out, q.numel(), "out"), (lse, batch * hq, "lse")):
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements; the call reads or writes {n}")
     _check(load().pgqa_decode_static_scratch(
         _dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), _dev(kv_indptr, "kv_indptr"),
         _dev(kv_indices, "kv_indices") if kv_indices.numel() else None, kv_indices.numel(),

@@ -108,3 +108,15 @@ def test_append_needs_a_slot_per_row():
     kp, vp = pools()
     with pytest.raises(ValueError, match="one slot per row"):
         B.kv_append(kp, vp, k, k, torch.zeros(2, dtype=torch.int64))
+
+
+@pytest.mark.parametrize("which", ["kv_indptr", "last_page_len", "out", "lse"])
+def test_static_scratch_needs_full_tables(which):
+    q = t(ROWS, HQ, D)
+    kp, vp = pools()
+    args = dict(kv_indptr=torch.zeros(ROWS + 1, dtype=torch.int32), kv_indices=torch.zeros(0, dtype=torch.int32),
+                last_page_len=torch.zeros(ROWS, dtype=torch.int32), out=torch.zeros(ROWS, HQ, D),
+                lse=torch.zeros(ROWS, HQ))
+    args[which] = args[which][:-1]
+    with pytest.raises(ValueError, match=which):
+        B.decode_static_scratch(q, kp, vp, splits=2, **args)
