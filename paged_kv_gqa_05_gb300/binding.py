@@ -261,6 +261,16 @@ def plan_update(plan: int, kv_indptr, last_page_len, kv_indices: torch.Tensor, n
                                    _stream(stream)))
 
 
+def _check_outputs(q: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor]) -> None:
+    """out holds a row for every row of q, and lse a value for every (row, head)."""
+    if q.dim() != 3:
+        raise ValueError("q must be [rows, num_qo_heads, head_dim]")
+    if out.numel() < q.numel():
+        raise ValueError(f"out holds {out.numel()} elements, q {q.numel()}")
+    if lse is not None and lse.numel() < q.shape[0] * q.shape[1]:
+        raise ValueError(f"lse holds {lse.numel()} elements, q has {q.shape[0] * q.shape[1]} (row, head) pairs")
+
+
 def run(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
         out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
         lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, pool_stable: bool = False,
@@ -271,6 +281,7 @@ def run(plan: int, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    _check_outputs(q, out, lse)
     if k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
         raise ValueError("q and pools must share one dtype")
     if pool_stable:
@@ -299,6 +310,7 @@ def append_run(plan: int, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Ten
         out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    _check_outputs(q, out, lse)
     for t, name in ((k_pool, "k_pool"), (v_pool, "v_pool"), (k_new, "k_new"), (v_new, "v_new")):
         if t.dtype != q.dtype:
             raise ValueError(f"{name} must have q's dtype")

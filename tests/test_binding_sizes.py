@@ -120,3 +120,20 @@ def test_static_scratch_needs_full_tables(which):
     args[which] = args[which][:-1]
     with pytest.raises(ValueError, match=which):
         B.decode_static_scratch(q, kp, vp, splits=2, **args)
+
+
+@pytest.mark.parametrize("which", ["out", "lse", "q"])
+def test_module_run_checks_outputs_against_q(which):
+    """The bare-handle calls cannot see the plan, but out and lse must cover q."""
+    q, out, lse = t(ROWS, HQ, D), torch.zeros(ROWS, HQ, D), torch.zeros(ROWS, HQ)
+    if which == "out":
+        out = out[:-1]
+    elif which == "lse":
+        lse = lse[:-1]
+    else:
+        q = q.reshape(ROWS, HQ * D)
+    kp, vp = pools()
+    with pytest.raises(ValueError, match=which):
+        B.run(1234, q, kp, vp, out=out, lse=lse)
+    with pytest.raises(ValueError, match=which):
+        B.append_run(1234, t(ROWS, HKV, D), t(ROWS, HKV, D), q, kp, vp, out=out, lse=lse)
