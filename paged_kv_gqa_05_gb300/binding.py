@@ -10,7 +10,6 @@ call raises.
 from __future__ import annotations
 
 import ctypes
-import inspect
 from pathlib import Path
 from typing import Optional
 
@@ -412,11 +411,6 @@ def read_device_flags(clear: bool = True) -> int:
     return int(v.value)
 
 
-_RUN_SIGNATURE = inspect.signature(run)
-_APPEND_RUN_SIGNATURE = inspect.signature(append_run)
-_UPDATE_SIGNATURE = inspect.signature(plan_update)
-
-
 class Plan:
     """Owns a plan handle; plan()/run() in the style of an attention backend.
 
@@ -434,35 +428,41 @@ class Plan:
     def _shape(self, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int) -> None:
         self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
         self.page_size = page_size
-        self._num_pages = None  # pool pages of the last successful update()
+        self._need = None  # elements per tensor that the last successful update() implies
 
-    def _check_sizes(self, arguments: dict) -> None:
-        if self._num_pages is None:
+    def _check_sizes(self, **tensors) -> None:
+        if self._need is None:
             return  # no successful update: the library refuses the call itself
-        rows = int(self.info()["total_q_rows"])
-        hq, hkv, d = self.num_qo_heads, self.num_kv_heads, self.head_dim
-        pool = self._num_pages * self.page_size * hkv * d
-        need = {"q": rows * hq * d, "out": rows * hq * d, "lse": rows * hq, "k_pool": pool, "v_pool": pool,
-                "k_new": rows * hkv * d, "v_new": rows * hkv * d}
-        for name, n in need.items():
-            t = arguments.get(name)
-            if isinstance(t, torch.Tensor) and t.numel() < n:
-                raise ValueError(f"{name} holds {t.numel()} elements; the plan reads or writes {n} "
-                                 f"({rows} query rows, {self._num_pages} pool pages)")
+        for name, t in tensors.items():
+            if t is not None and t.numel() < self._need[name]:
+                raise ValueError(f"{name} holds {t.numel()} elements; the plan reads or writes "
+                                 f"{self._need[name]} ({self._rows} query rows, {self._num_pages} pool pages)")
 
-    def update(self, *args, **kwargs) -> "Plan":
-        self._num_pages = None
-        plan_update(self.handle, *args, **kwargs)
-        self._num_pages = int(_UPDATE_SIGNATURE.bind(self.handle, *args, **kwargs).arguments["num_pages"])
+    def update(self, kv_indptr, last_page_len, kv_indices: torch.Tensor, num_pages: int, **kwargs) -> "Plan":
+        self._need = None
+        plan_update(self.handle, kv_indptr, last_page_len, kv_indices, num_pages, **kwargs)
+        rows, pages = int(self.info()["total_q_rows"]), int(num_pages)
+        hq, hkv, d = self.num_qo_heads, self.num_kv_heads, self.head_dim
+        pool = pages * self.page_size * hkv * d
+        self._rows, self._num_pages = rows, pages
+        self._need = {"q": rows * hq * d, "out": rows * hq * d, "lse": rows * hq, "k_pool": pool, "v_pool": pool,
+                      "k_new": rows * hkv * d, "v_new": rows * hkv * d}
         return self
 
-    def run(self, *args, **kwargs) -> torch.Tensor:
-        self._check_sizes(_RUN_SIGNATURE.bind(self.handle, *args, **kwargs).arguments)
-        return run(self.handle, *args, **kwargs)
+    def run(self, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, out: Optional[torch.Tensor] = None,
+            out_dtype: Optional[torch.dtype] = None, lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0,
+            pool_stable: bool = False, stream=None) -> torch.Tensor:
+        self._check_sizes(q=q, k_pool=k_pool, v_pool=v_pool, out=out, lse=lse)
+        return run(self.handle, q, k_pool, v_pool, out=out, out_dtype=out_dtype, lse=lse, sm_scale=sm_scale,
+                   pool_stable=pool_stable, stream=stream)
 
-    def append_run(self, *args, **kwargs) -> torch.Tensor:
-        self._check_sizes(_APPEND_RUN_SIGNATURE.bind(self.handle, *args, **kwargs).arguments)
-        return append_run(self.handle, *args, **kwargs)
+    def append_run(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, k_pool: torch.Tensor,
+                   v_pool: torch.Tensor, out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+                   lse: Optional[torch.Tensor] = None, sm_scale: float = 0.0, pool_stable: bool = False,
+                   stream=None) -> torch.Tensor:
+        self._check_sizes(k_new=k_new, v_new=v_new, q=q, k_pool=k_pool, v_pool=v_pool, out=out, lse=lse)
+        return append_run(self.handle, k_new, v_new, q, k_pool, v_pool, out=out, out_dtype=out_dtype, lse=lse,
+                          sm_scale=sm_scale, pool_stable=pool_stable, stream=stream)
 
     def kv_append_rope(self, *args, **kwargs) -> None:
         kv_append_rope(self.handle, *args, **kwargs)
