@@ -428,25 +428,28 @@ class Plan:
     def _shape(self, num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int) -> None:
         self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
         self.page_size = page_size
-        self._need = None  # elements per tensor that the last successful update() implies
+        self._num_pages = None  # pool pages of the last successful update()
+        self._need = None       # elements per tensor that update implies (computed on first use)
 
     def _check_sizes(self, **tensors) -> None:
-        if self._need is None:
+        if self._num_pages is None:
             return  # no successful update: the library refuses the call itself
+        if self._need is None:
+            rows = int(self.info()["total_q_rows"])
+            hq, hkv, d = self.num_qo_heads, self.num_kv_heads, self.head_dim
+            pool = self._num_pages * self.page_size * hkv * d
+            self._rows = rows
+            self._need = {"q": rows * hq * d, "out": rows * hq * d, "lse": rows * hq, "k_pool": pool,
+                          "v_pool": pool, "k_new": rows * hkv * d, "v_new": rows * hkv * d}
         for name, t in tensors.items():
             if t is not None and t.numel() < self._need[name]:
                 raise ValueError(f"{name} holds {t.numel()} elements; the plan reads or writes "
                                  f"{self._need[name]} ({self._rows} query rows, {self._num_pages} pool pages)")
 
     def update(self, kv_indptr, last_page_len, kv_indices: torch.Tensor, num_pages: int, **kwargs) -> "Plan":
-        self._need = None
+        self._num_pages, self._need = None, None
         plan_update(self.handle, kv_indptr, last_page_len, kv_indices, num_pages, **kwargs)
-        rows, pages = int(self.info()["total_q_rows"]), int(num_pages)
-        hq, hkv, d = self.num_qo_heads, self.num_kv_heads, self.head_dim
-        pool = pages * self.page_size * hkv * d
-        self._rows, self._num_pages = rows, pages
-        self._need = {"q": rows * hq * d, "out": rows * hq * d, "lse": rows * hq, "k_pool": pool, "v_pool": pool,
-                      "k_new": rows * hkv * d, "v_new": rows * hkv * d}
+        self._num_pages = int(num_pages)
         return self
 
     def run(self, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, out: Optional[torch.Tensor] = None,
