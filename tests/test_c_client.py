@@ -87,3 +87,18 @@ def test_c_program_gets_the_binding_schedule(tmp_path):
     assert lines[1:-1] == want
     assert info["num_merge_tasks"] == 2  # the 300-key request is split for both kv heads
     assert lines[-1].startswith("bad malformed page table | kv_indices[5] = 24 outside [0, 24)")
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs a C++ compiler")
+def test_header_compiles_as_cpp(tmp_path):
+    """The same client builds as C++11 (the header's extern "C" block), warnings as errors."""
+    lib = build.build()
+    src = tmp_path / "client.cpp"
+    src.write_text(CLIENT)
+    exe = tmp_path / "client_cpp"
+    subprocess.run(["g++", "-std=c++11", "-Wall", "-Wextra", "-Werror", "-pedantic", f"-I{ROOT / 'include'}",
+                    str(src), "-o", str(exe), f"-L{lib.parent}", "-lpagedgqa", f"-Wl,-rpath,{lib.parent}"],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    assert out.startswith("info ") and "bad malformed page table" in out
+
