@@ -1,6 +1,6 @@
 """CPU tests of bench.py's host logic: the multi-rank plumbing (world size 2 over
-gloo: barrier, max/sum over ranks, rank-0-only reporting) and the reference arm
-(the CPU oracle) JSON line."""
+gloo: barrier, max/sum over ranks, rank-0-only reporting), the reference arm
+(the CPU oracle) JSON line, the ncu traffic lookup and the clock record."""
 import json
 import os
 import socket
@@ -89,3 +89,48 @@ def test_profiled_traffic_lookup(tmp_path, monkeypatch):
     assert bench.profiled_traffic("w") == 123
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda sources=(): "1")
     assert bench.profiled_traffic("w") is None
+
+
+class _Stopped:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_record_keeps_this_gpu_and_its_throttle_reasons(tmp_path):
+    """The clock sampler's summary: only this GPU's rows (by UUID), the median SM clock,
+    the highest max clock and every throttle reason seen active."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rows = [
+        "GPU-aaaa, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-bbbb, 600, 2070, 200.0, 0x8, Active, Not Active, Not Active, Not Active",
+        "GPU-aaaa, 2010, 2070, 1100.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "GPU-aaaa, 1980, 2070, 1010.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-aaaa, [N/A], 2070, 990.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc, s.path, s.uuid = _Stopped(), str(path), "aaaa"
+    rec = s.stop()
+    assert rec["sm_mhz"] == 1980.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"]  # the other GPU's hw_slowdown is not ours
+    assert rec["samples"] == 4 and rec["power_w_max"] == 1100.5
+    assert not path.exists()
+
+
+def test_clock_record_without_samples(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc = None
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+    path = tmp_path / "clocks.csv"
+    path.write_text("GPU-bbbb, 600, 2070, 200.0, 0x8, Active, Not Active, Not Active, Not Active\n"
+                    "GPU-cccc, 600, 2070, 200.0, 0x8, Active, Not Active, Not Active, Not Active\n")
+    s.proc, s.path, s.uuid = _Stopped(), str(path), "aaaa"
+    assert s.stop()["reasons"] == ["no samples for this GPU"]
