@@ -1,4 +1,4 @@
-"""Thin ctypes binding of libpagedgqa.so (argument marshalling only).
+"""Thin ctypes binding of libpagedgqa.so (argument marshalling and size checks only).
 
 The functions carry the C ABI's names without the ``pgqa_`` prefix:
 ``kv_append``, ``plan_create``, ``plan_update``, ``run``, ``plan_destroy``,
